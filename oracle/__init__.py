@@ -1,0 +1,21 @@
+"""CPU oracle for paged varlen attention -- TEST INFRASTRUCTURE, NOT THE PRODUCT.
+
+A plain fp64 C implementation (``pa_oracle.c``) of what the hot path computes,
+loaded through ctypes.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import this package; the CUDA
+library and its Python binding never do.
+
+Functions mirror the library's calls but take numpy arrays and return float64:
+  reshape_and_cache(...)        byte-exact scatter (returns new pool arrays)
+  paged_attention(w, rows=...)  fp64 attention for selected query rows
+  split_partials / split_combine  the split-KV partials and shared reduce
+"""
+from .oracle import (  # noqa: F401
+    build_oracle,
+    attention_of,
+    paged_attention,
+    reshape_and_cache,
+    split_combine,
+    split_partials,
+    library_path,
+)
