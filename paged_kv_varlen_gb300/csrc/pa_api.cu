@@ -1,0 +1,377 @@
+// pa_api.cu -- the C ABI (include/pa.h): host-side argument checks, the
+// split-KV plan, TMA tensor maps over the page pool, and the launch sequence
+// of one attention call.  Everything here is host code except the device
+// error word.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+#define PA_API extern "C" __attribute__((visibility("default")))
+
+namespace pa {
+namespace {
+
+// The device error word of this library: one int per device that loads it,
+// read and cleared by pa_device_error().
+__device__ int g_error_word;
+
+thread_local char g_last_error[256] = "no error";
+
+pa_status cuda_fail(cudaError_t e, const char *where) {
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e),
+             cudaGetErrorString(e));
+    return PA_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int *err = nullptr;
+    bool ready = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// SM count and error-word address of the current device (looked up once).
+pa_status device_info(DeviceInfo *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_error_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+        d.ready = true;
+    }
+    *out = d;
+    return PA_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda
+// link dependency).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// A 3-D map over one cache: x = element within a head row (D), y = KV head,
+// z = token row of the pool (page * block_size + slot).  Boxes are 128 bytes
+// wide (one swizzle span) and `box_rows` rows tall, 128-byte swizzled.
+pa_status make_cache_map(CUtensorMap *map, const void *cache, pa_dtype dtype, int head_dim,
+                         int num_kv_heads, int64_t pool_rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled unavailable");
+        return PA_ERR_CUDA;
+    }
+    const int e = dtype == PA_F32 ? 4 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)pool_rows};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * e, (cuuint64_t)head_dim * num_kv_heads * e};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / e), 1, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, dtype == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    3, const_cast<void *>(cache), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Split-KV workspace layout: part_o, then part_m, then part_l.
+struct SplitLayout {
+    size_t o_bytes, ml_bytes, total;
+};
+
+SplitLayout split_layout(int num_seqs, int max_parts, int num_q_heads, int head_dim) {
+    SplitLayout L;
+    const size_t units = (size_t)num_seqs * max_parts * num_q_heads;
+    L.o_bytes = align256(units * head_dim * sizeof(float));
+    L.ml_bytes = align256(units * sizeof(float));
+    L.total = L.o_bytes + 2 * L.ml_bytes;
+    return L;
+}
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+PA_API const char *pa_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+PA_API const char *pa_last_error_string(void) { return g_last_error; }
+
+PA_API const char *pa_build_info(void) {
+    return "libpa paged varlen attention; sm_103a; kernels: reshape_and_cache, "
+           "paged_decode (TMA ring, CUDA cores), split_reduce";
+}
+
+PA_API int pa_choose_partition_size(int num_seqs, int num_kv_heads, int max_seqlen_k,
+                                    int partition_size, int sm_count) {
+    if (partition_size < 0) return 0;
+    if (partition_size > 0) return partition_size;
+    if (max_seqlen_k <= 512) return 0;
+    // Work budget: keep every SM busy with several CTAs of whole partitions.
+    // Long partitions first (less partial traffic), shorter when the batch is
+    // too small to fill the GPU (the page's 512-then-256 order).
+    const int64_t units = (int64_t)num_seqs * num_kv_heads;
+    const int64_t want = (int64_t)4 * (sm_count > 0 ? sm_count : 148);
+    if (units >= want && max_seqlen_k <= 2048) return 0;
+    if (units * (max_seqlen_k / 512) >= want) return 512;
+    return 256;
+}
+
+PA_API size_t pa_varlen_attention_workspace_size(int num_seqs, int max_seqlen_k,
+                                                 int num_q_heads, int head_dim,
+                                                 int partition_size) {
+    if (partition_size < 0 || num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    const int P = partition_size > 0 ? partition_size : 256;  // auto picks 0, 256 or 512
+    const int max_parts = max_seqlen_k > 0 ? ceil_div(max_seqlen_k, P) : 1;
+    return split_layout(num_seqs, max_parts, num_q_heads, head_dim).total;
+}
+
+PA_API pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t kv_token_stride,
+                                      void *key_cache, void *value_cache,
+                                      const int64_t *slot_mapping, int64_t num_tokens,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int64_t num_blocks, pa_dtype dtype, void *stream) {
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (kv_token_stride < (int64_t)num_kv_heads * head_dim) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    const int64_t e = dtype == PA_F32 ? 4 : 2;
+    if (((reinterpret_cast<uintptr_t>(key) | reinterpret_cast<uintptr_t>(value) |
+          reinterpret_cast<uintptr_t>(key_cache) | reinterpret_cast<uintptr_t>(value_cache)) %
+         e) != 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens > (int64_t)0x7fffffff * 8) return PA_ERR_UNSUPPORTED;
+    cudaError_t err = launch_reshape_and_cache(
+        key, value, kv_token_stride * e, key_cache, value_cache, slot_mapping, num_tokens,
+        (int64_t)num_kv_heads * head_dim * e, num_blocks * block_size,
+        static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "reshape_and_cache launch");
+    return PA_OK;
+}
+
+PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_cache,
+                                     const void *value_cache, const int32_t *cu_seqlens_q,
+                                     const int32_t *seq_lens_k, const int32_t *block_tables,
+                                     int max_blocks_per_seq, int num_seqs, int64_t total_q,
+                                     int max_seqlen_q, int max_seqlen_k, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int block_size,
+                                     int64_t num_blocks, float scale, const float *sinks,
+                                     int causal, int partition_size, void *workspace,
+                                     size_t workspace_bytes, pa_dtype dtype, void *stream) {
+    // ---- host-side checks (nothing is launched if one fails)
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+        return PA_ERR_INVALID_ARG;
+    if (total_q == 0) return PA_OK;
+    if (num_seqs == 0) return PA_ERR_INVALID_ARG;
+    if (!out || !q || !key_cache || !value_cache || !cu_seqlens_q || !seq_lens_k || !block_tables)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq <= 0 || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
+    if (partition_size < -1 || (partition_size > 0 && partition_size % 32 != 0))
+        return PA_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    if (group > 8) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (block_size % 8 != 0 || block_size > 1024) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (num_blocks * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    if (total_q > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    if (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3)) return PA_ERR_INVALID_ARG;
+
+    DeviceInfo dev;
+    pa_status st = device_info(&dev);
+    if (st != PA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // ---- split plan and workspace
+    const int P = pa_choose_partition_size(num_seqs, num_kv_heads, max_seqlen_k, partition_size,
+                                           dev.sm_count);
+    const int max_parts = (P > 0 && max_seqlen_k > 0) ? ceil_div(max_seqlen_k, P) : 1;
+    float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
+    if (P > 0) {
+        const SplitLayout L = split_layout(num_seqs, max_parts, num_q_heads, head_dim);
+        if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
+            return PA_ERR_WORKSPACE;
+        part_o = static_cast<float *>(workspace);
+        part_m = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.o_bytes);
+        part_l = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.o_bytes + L.ml_bytes);
+    }
+
+    // ---- tensor maps over the two caches
+    const int e = dtype == PA_F32 ? 4 : 2;
+    const int box_rows = gcd_int(decode_tile_keys(e, head_dim), block_size);
+    CUtensorMap kmap, vmap;
+    st = make_cache_map(&kmap, key_cache, dtype, head_dim, num_kv_heads, num_blocks * block_size,
+                        box_rows);
+    if (st != PA_OK) return st;
+    st = make_cache_map(&vmap, value_cache, dtype, head_dim, num_kv_heads,
+                        num_blocks * block_size, box_rows);
+    if (st != PA_OK) return st;
+
+    DecodeArgs a;
+    memset(&a, 0, sizeof a);
+    a.out = out;
+    a.q = q;
+    a.cu_seqlens_q = cu_seqlens_q;
+    a.seq_lens_k = seq_lens_k;
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.qscale = scale * kLog2e;
+    a.sinks = sinks;
+    a.causal = causal ? 1 : 0;
+    a.partition_size = P;
+    a.max_parts = max_parts;
+    a.part_o = part_o;
+    a.part_m = part_m;
+    a.part_l = part_l;
+    a.total_q = total_q;
+    a.err = dev.err;
+
+    auto launch = [&](dim3 grid) -> cudaError_t {
+        if (dtype == PA_F32) {
+            switch (head_dim) {
+                case 64: return launch_decode_f32_d64(group, kmap, vmap, a, grid, s);
+                case 128: return launch_decode_f32_d128(group, kmap, vmap, a, grid, s);
+                default: return launch_decode_f32_d256(group, kmap, vmap, a, grid, s);
+            }
+        }
+        switch (head_dim) {
+            case 64: return launch_decode_bf16_d64(group, kmap, vmap, a, grid, s);
+            case 128: return launch_decode_bf16_d128(group, kmap, vmap, a, grid, s);
+            default: return launch_decode_bf16_d256(group, kmap, vmap, a, grid, s);
+        }
+    };
+
+    // 1) single-query requests (decode): (partition, kv head, request) CTAs
+    a.mode = 0;
+    cudaError_t ce = launch(dim3(max_parts, num_kv_heads, num_seqs));
+    if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode launch");
+    // 2) rows of multi-query requests (verify windows, prefill chunks)
+    if (max_seqlen_q > 1) {
+        a.mode = 1;
+        ce = launch(dim3((unsigned)total_q, num_kv_heads, 1));
+        if (ce != cudaSuccess) return cuda_fail(ce, "paged_rows launch");
+    }
+    // 3) merge the split partials of the single-query requests
+    if (P > 0) {
+        ReduceArgs ra;
+        ra.out = out;
+        ra.part_o = part_o;
+        ra.part_m = part_m;
+        ra.part_l = part_l;
+        ra.cu_seqlens_q = cu_seqlens_q;
+        ra.seq_lens_k = seq_lens_k;
+        ra.num_seqs = num_seqs;
+        ra.max_parts = max_parts;
+        ra.partition_size = P;
+        ra.num_q_heads = num_q_heads;
+        ra.sinks = sinks;
+        ce = launch_reduce(e, head_dim, ra, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "split_reduce launch");
+    }
+    return PA_OK;
+}
+
+PA_API pa_status pa_split_kv_reduce(void *out, const float *part_out, const float *part_max,
+                                    const float *part_sum, const int32_t *cu_seqlens_q,
+                                    const int32_t *seq_lens_k, int num_seqs, int max_parts,
+                                    int partition_size, int num_q_heads, int head_dim,
+                                    const float *sinks, pa_dtype dtype, void *stream) {
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (num_seqs < 0 || max_parts <= 0 || partition_size <= 0 || num_q_heads <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (num_seqs > 0x7fffffff || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (max_parts > 12288) return PA_ERR_UNSUPPORTED;   // weights live in shared memory
+    if (!out || !part_out || !part_max || !part_sum || !cu_seqlens_q || !seq_lens_k)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(part_out) || (reinterpret_cast<uintptr_t>(out) & 3)) return PA_ERR_INVALID_ARG;
+    ReduceArgs ra;
+    ra.out = out;
+    ra.part_o = part_out;
+    ra.part_m = part_max;
+    ra.part_l = part_sum;
+    ra.cu_seqlens_q = cu_seqlens_q;
+    ra.seq_lens_k = seq_lens_k;
+    ra.num_seqs = num_seqs;
+    ra.max_parts = max_parts;
+    ra.partition_size = partition_size;
+    ra.num_q_heads = num_q_heads;
+    ra.sinks = sinks;
+    cudaError_t ce = launch_reduce(dtype == PA_F32 ? 4 : 2, head_dim, ra,
+                                   static_cast<cudaStream_t>(stream));
+    if (ce != cudaSuccess) return cuda_fail(ce, "split_reduce launch");
+    return PA_OK;
+}
+
+PA_API pa_status pa_device_error(int *code) {
+    if (!code) return PA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    pa_status st = device_info(&dev);
+    if (st != PA_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    e = cudaMemcpy(code, dev.err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    const int zero = 0;
+    e = cudaMemcpy(dev.err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+    return PA_OK;
+}

@@ -1,0 +1,84 @@
+// pa_internal.h -- host-side structures shared between the C-ABI layer
+// (pa_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
+
+// Arguments of the paged decode / multi-row kernel (CUDA cores).
+struct DecodeArgs {
+    void *out;                 // [total_q, Hq, D]
+    const void *q;             // [total_q, Hq, D]
+    const int32_t *cu_seqlens_q;
+    const int32_t *seq_lens_k;
+    const int32_t *block_tables;
+    int max_blocks_per_seq;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int block_size;
+    float qscale;              // scale * log2(e)
+    const float *sinks;        // [Hq] or nullptr
+    int causal;
+    // mode 0: grid (max_parts, Hkv, num_seqs); single-query requests only.
+    // mode 1: grid (total_q, Hkv); rows of multi-query requests only.
+    int mode;
+    int partition_size;        // mode 0: > 0 writes split partials, 0 = whole range
+    int max_parts;
+    float *part_o;             // [num_seqs, max_parts, Hq, D]
+    float *part_m;             // [num_seqs, max_parts, Hq]
+    float *part_l;             // [num_seqs, max_parts, Hq]
+    int64_t total_q;
+    int *err;                  // device error word
+};
+
+struct ReduceArgs {
+    void *out;
+    const float *part_o;
+    const float *part_m;
+    const float *part_l;
+    const int32_t *cu_seqlens_q;
+    const int32_t *seq_lens_k;
+    int num_seqs;
+    int max_parts;
+    int partition_size;
+    int num_q_heads;
+    const float *sinks;
+};
+
+// Per (dtype, head_dim) launchers; `group` = Hq / Hkv in 1..8.
+// Each returns the launch error (cudaSuccess if launched).
+#define PA_DECLARE_DECODE(NAME) \
+    cudaError_t NAME(int group, const CUtensorMap &kmap, const CUtensorMap &vmap, \
+                     const DecodeArgs &a, dim3 grid, cudaStream_t stream);
+PA_DECLARE_DECODE(launch_decode_f32_d64)
+PA_DECLARE_DECODE(launch_decode_f32_d128)
+PA_DECLARE_DECODE(launch_decode_f32_d256)
+PA_DECLARE_DECODE(launch_decode_bf16_d64)
+PA_DECLARE_DECODE(launch_decode_bf16_d128)
+PA_DECLARE_DECODE(launch_decode_bf16_d256)
+#undef PA_DECLARE_DECODE
+
+// Keys per tile of the decode kernel: 32 keys for rows of up to 256 bytes
+// (one lane per key), 16 for 512-byte rows, 8 for 1024-byte rows.
+__host__ __device__ constexpr int decode_tile_keys(int elem_bytes, int head_dim) {
+    return head_dim * elem_bytes <= 256 ? 32 : (head_dim * elem_bytes == 512 ? 16 : 8);
+}
+
+// gcd of the tile length and the block size: the rows one TMA box copies, so
+// that a box never crosses a page boundary.
+__host__ __device__ constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
+
+cudaError_t launch_reduce(int elem_bytes, int head_dim, const ReduceArgs &a, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t stride_bytes,
+                                     void *key_cache, void *value_cache, const int64_t *slots,
+                                     int64_t num_tokens, int64_t row_bytes, int64_t num_slots,
+                                     cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,117 @@
+// reduce.cu -- the shared split-KV reduce (kwkr.cn trick 4: partials are a
+// log2-space (max, exp-sum) pair plus a normalised partial output; one shared
+// reduce kernel merges them, and the GQA decode path reuses it).
+//
+// One CTA per (request, query head).  The partition weights
+// w_p = l_p * 2^(m_p - M) are computed once into shared memory, then each
+// thread combines a 16-byte slice of the head dimension across partitions
+// (coalesced reads of the [num_seqs, max_parts, Hq, D] partial outputs).
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr int kReduceThreads = 128;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const ReduceArgs a) {
+    extern __shared__ float wsh[];   // [max_parts] weights
+    __shared__ float red[kReduceThreads / 32];
+    __shared__ float Msh, densh;
+    const int r = blockIdx.x;
+    const int hq = blockIdx.y;
+    const int Hq = a.num_q_heads;
+    const int c0 = a.cu_seqlens_q[r];
+    if (a.cu_seqlens_q[r + 1] - c0 != 1) return;
+    const int N = max(0, a.seq_lens_k[r]);
+    const int nparts = min((N + a.partition_size - 1) / a.partition_size, a.max_parts);
+    const int tid = threadIdx.x;
+    const float sk2 = a.sinks ? a.sinks[hq] * kLog2e : -INFINITY;
+
+    // M = max over partitions of m_p, and over the sink logit
+    float mx = -INFINITY;
+    for (int p = tid; p < nparts; p += kReduceThreads)
+        mx = fmaxf(mx, a.part_m[((int64_t)r * a.max_parts + p) * Hq + hq]);
+    mx = warp_max(mx);
+    if ((tid & 31) == 0) red[tid >> 5] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        float M = sk2;
+        for (int w = 0; w < kReduceThreads / 32; ++w) M = fmaxf(M, red[w]);
+        Msh = M;
+    }
+    __syncthreads();
+    const float M = Msh;
+    float sum = 0.f;
+    for (int p = tid; p < nparts; p += kReduceThreads) {
+        const int64_t slot = ((int64_t)r * a.max_parts + p) * Hq + hq;
+        const float w = a.part_l[slot] * exp2f(a.part_m[slot] - M);
+        wsh[p] = w;
+        sum += w;
+    }
+    sum = warp_sum(sum);
+    __syncthreads();   // red[] reuse
+    if ((tid & 31) == 0) red[tid >> 5] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int w = 0; w < kReduceThreads / 32; ++w) s += red[w];
+        if (a.sinks && nparts > 0) s += exp2f(sk2 - M);
+        densh = s;
+    }
+    __syncthreads();
+    const float den = densh;
+
+    constexpr int VEC = 4;
+    constexpr int LANES = D / VEC;
+    T *out = reinterpret_cast<T *>(a.out) + ((int64_t)c0 * Hq + hq) * D;
+    for (int c = tid; c < LANES; c += kReduceThreads) {
+        float acc[VEC] = {0.f, 0.f, 0.f, 0.f};
+        for (int p = 0; p < nparts; ++p) {
+            const float w = wsh[p];
+            const float4 o = *reinterpret_cast<const float4 *>(
+                a.part_o + (((int64_t)r * a.max_parts + p) * Hq + hq) * D + c * VEC);
+            acc[0] = fmaf(w, o.x, acc[0]);
+            acc[1] = fmaf(w, o.y, acc[1]);
+            acc[2] = fmaf(w, o.z, acc[2]);
+            acc[3] = fmaf(w, o.w, acc[3]);
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            out[c * VEC + e] = Elem<T>::to_store(nparts > 0 ? acc[e] / den : 0.f);
+    }
+}
+
+template <typename T, int D>
+static cudaError_t launch_reduce_t(const ReduceArgs &a, cudaStream_t stream) {
+    const size_t smem = sizeof(float) * (size_t)(a.max_parts > 0 ? a.max_parts : 1);
+    auto kern = split_reduce_kernel<T, D>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid(a.num_seqs, a.num_q_heads);
+    kern<<<grid, kReduceThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(int elem_bytes, int head_dim, const ReduceArgs &a, cudaStream_t stream) {
+    if (a.num_seqs == 0 || a.num_q_heads == 0) return cudaSuccess;
+    if (elem_bytes == 4) {
+        switch (head_dim) {
+            case 64: return launch_reduce_t<float, 64>(a, stream);
+            case 128: return launch_reduce_t<float, 128>(a, stream);
+            case 256: return launch_reduce_t<float, 256>(a, stream);
+        }
+    } else {
+        switch (head_dim) {
+            case 64: return launch_reduce_t<__nv_bfloat16, 64>(a, stream);
+            case 128: return launch_reduce_t<__nv_bfloat16, 128>(a, stream);
+            case 256: return launch_reduce_t<__nv_bfloat16, 256>(a, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

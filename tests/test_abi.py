@@ -1,0 +1,115 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every entry point
+that include/pa.h declares, and its host-only logic (status names, workspace
+size, partition plan, argument checks that return before any CUDA call)
+behaves as documented.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_varlen_gb300 import build
+    from paged_kv_varlen_gb300 import binding
+    build.build_library()
+    return binding.load_library()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_three_hot_path_calls():
+    names = declared_functions()
+    for n in ("pa_reshape_and_cache", "pa_varlen_attention", "pa_split_kv_reduce"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_status_strings_and_build_info(lib):
+    assert lib.pa_status_string(0) == b"PA_OK"
+    assert lib.pa_status_string(3) == b"PA_ERR_WORKSPACE"
+    assert b"sm_103a" in lib.pa_build_info()
+
+
+def test_workspace_size(lib):
+    # forced P = 512: 4 seqs x ceil(8192/512)=16 parts x 32 heads x (128 + 2) floats
+    n = lib.pa_varlen_attention_workspace_size(4, 8192, 32, 128, 512)
+    units = 4 * 16 * 32
+    assert n >= units * (128 + 2) * 4
+    assert n < units * (128 + 2) * 4 + 3 * 256
+    assert lib.pa_varlen_attention_workspace_size(4, 8192, 32, 128, -1) == 0
+    # auto is bounded by the smallest partition it may choose (256)
+    assert (lib.pa_varlen_attention_workspace_size(4, 8192, 32, 128, 0)
+            >= lib.pa_varlen_attention_workspace_size(4, 8192, 32, 128, 256))
+
+
+def test_partition_plan(lib):
+    f = lib.pa_choose_partition_size
+    assert f(32, 8, 8193, -1, 152) == 0         # never split
+    assert f(32, 8, 8193, 512, 152) == 512      # forced
+    assert f(32, 8, 300, 0, 152) == 0           # short contexts: no split
+    assert f(32, 8, 8192, 0, 152) == 512        # enough work with 512-key partitions
+    assert f(2, 4, 65536, 0, 152) in (256, 512)
+    assert f(1, 1, 4096, 0, 152) == 256         # tiny batch: shorter partitions
+
+
+def _call_attention(lib, **over):
+    args = dict(out=16, q=16, kc=16, vc=16, cu=16, sl=16, bt=16, mbps=4, S=2, total_q=2,
+                mq=1, mk=40, Hq=4, Hkv=2, D=64, bs=16, nb=16, scale=0.125, sinks=None,
+                causal=1, P=0, ws=None, ws_bytes=0, dtype=0, stream=None)
+    args.update(over)
+    v = ctypes.c_void_p
+    return lib.pa_varlen_attention(
+        v(args["out"]), v(args["q"]), v(args["kc"]), v(args["vc"]), v(args["cu"]), v(args["sl"]),
+        v(args["bt"]), args["mbps"], args["S"], args["total_q"], args["mq"], args["mk"],
+        args["Hq"], args["Hkv"], args["D"], args["bs"], args["nb"], args["scale"],
+        args["sinks"], args["causal"], args["P"], args["ws"], args["ws_bytes"], args["dtype"],
+        args["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(out=0), 1),                 # null output
+    (dict(dtype=7), 1),               # unknown dtype
+    (dict(Hq=5), 1),                  # H_q not a multiple of H_kv
+    (dict(Hq=18, Hkv=2), 2),          # group of 9 > 8
+    (dict(D=96), 2),                  # head_dim not compiled
+    (dict(bs=12), 2),                 # block size not a multiple of 8
+    (dict(P=100), 1),                 # partition not a multiple of 32
+    (dict(q=24), 1),                  # misaligned query pointer
+    (dict(S=0), 1),                   # rows without requests
+    (dict(total_q=0), 0),             # nothing to do
+])
+def test_attention_argument_checks_return_before_any_launch(lib, over, status):
+    assert _call_attention(lib, **over) == status
+
+
+def test_scatter_argument_checks(lib):
+    v = ctypes.c_void_p
+    f = lib.pa_reshape_and_cache
+    assert f(v(16), v(16), 128, v(16), v(16), v(16), 0, 2, 64, 16, 8, 1, None) == 0   # no tokens
+    assert f(v(16), v(16), 100, v(16), v(16), v(16), 4, 2, 64, 16, 8, 1, None) == 1   # stride < H*D
+    assert f(None, v(16), 128, v(16), v(16), v(16), 4, 2, 64, 16, 8, 1, None) == 1    # null key
+    assert f(v(16), v(16), 128, v(16), v(16), v(16), 4, 2, 64, 16, 8, 9, None) == 1   # dtype
+
+
+def test_reduce_argument_checks(lib):
+    v = ctypes.c_void_p
+    f = lib.pa_split_kv_reduce
+    assert f(v(16), v(16), v(16), v(16), v(16), v(16), 2, 4, 256, 4, 96, None, 1, None) == 2
+    assert f(v(16), v(16), v(16), v(16), v(16), v(16), 2, 0, 256, 4, 64, None, 1, None) == 1
+    assert f(None, v(16), v(16), v(16), v(16), v(16), 2, 4, 256, 4, 64, None, 1, None) == 1
