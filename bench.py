@@ -206,7 +206,7 @@ def cpu_baseline(w, budget_s=12.0):
     prepare_oracle_pool(w)
     rows = np.arange(w.total_q)
     t, n = 0.0, 0
-    while t < budget_s and n < 8:
+    while t < budget_s and n < 1000:
         t += time_oracle(w, rows, nthreads)
         n += 1
     gbs = n * row_bytes(w, rows) / t / 1e9
