@@ -181,6 +181,41 @@ pa_status pa_split_kv_reduce(void *out, const float *part_out, const float *part
                              int partition_size, int num_q_heads, int head_dim,
                              const float *sinks, pa_dtype dtype, void *stream);
 
+/* Bytes of the fixed device scratch behind pa_varlen_attention_static_scratch. */
+#define PA_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * pa_varlen_attention_static_scratch -- pa_varlen_attention for callers that
+ * cannot allocate device memory.  (The pages have no counterpart: it exists
+ * for callers such as a host framework that owns every device allocation, a
+ * serving loop that must never stall or synchronise on cudaMalloc/cudaFree,
+ * or a plugin with no allocator at all; they cannot pass a workspace.)
+ *
+ * Same arguments and results as pa_varlen_attention, minus the workspace.
+ * The split-KV partials live in a scratch array of PA_STATIC_SCRATCH_BYTES
+ * (16 MiB) compiled into the library as device memory: every GPU that loads
+ * the library holds it until the process exits.  The call itself allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture.
+ *  - A call whose split plan needs more than PA_STATIC_SCRATCH_BYTES returns
+ *    PA_ERR_WORKSPACE without launching anything (pa_last_error_string() says
+ *    how many bytes it needed); use pa_varlen_attention with a workspace, a
+ *    longer partition_size, or partition_size = -1 instead.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Nothing in it needs to start at zero (a call reads only partials it has
+ *    written), but calls that overlap on the GPU -- on two streams, or from
+ *    two threads -- race on it: order them on one stream.
+ */
+pa_status pa_varlen_attention_static_scratch(
+    void *out, const void *q, const void *key_cache, const void *value_cache,
+    const int32_t *cu_seqlens_q, const int32_t *seq_lens_k, const int32_t *block_tables,
+    int max_blocks_per_seq, int num_seqs, int64_t total_q, int max_seqlen_q, int max_seqlen_k,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+    float scale, const float *sinks, int causal, int partition_size, pa_dtype dtype,
+    void *stream);
+
 /*
  * Reads and clears the library's device-side error word for the current
  * device (synchronises the device).  Nonzero means a kernel gave up on a

@@ -178,3 +178,30 @@ def pa_device_error() -> int:
     code = ctypes.c_int(0)
     _check(load_library().pa_device_error(ctypes.byref(code)), "pa_device_error")
     return code.value
+
+
+def pa_varlen_attention_static_scratch(out: torch.Tensor, q: torch.Tensor,
+                                       key_cache: torch.Tensor, value_cache: torch.Tensor,
+                                       cu_seqlens_q: torch.Tensor, seq_lens_k: torch.Tensor,
+                                       block_tables: torch.Tensor, *, max_seqlen_q: int,
+                                       max_seqlen_k: int, scale: float,
+                                       sinks: Optional[torch.Tensor] = None, causal: bool = True,
+                                       partition_size: int = 0, stream=None) -> torch.Tensor:
+    """pa_varlen_attention without a workspace, for callers that must not
+    allocate device memory: the split-KV partials go to the library's fixed
+    16 MiB device scratch (shared by all calls; order overlapping calls on one
+    stream).  Raises PAError (PA_ERR_WORKSPACE) when a call needs more."""
+    lib = load_library()
+    fn = lib.pa_varlen_attention_static_scratch
+    if fn.argtypes is None:
+        P, I, L, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        fn.restype = I
+        fn.argtypes = [P, P, P, P, P, P, P, I, I, L, I, I, I, I, I, I, L, F, P, I, I, I, P]
+    total_q, Hq, D = q.shape
+    nb, bs, Hkv, _ = key_cache.shape
+    st = fn(_ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(cu_seqlens_q),
+            _ptr(seq_lens_k), _ptr(block_tables), block_tables.shape[1], seq_lens_k.shape[0],
+            total_q, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, bs, nb, float(scale),
+            _ptr(sinks), int(bool(causal)), int(partition_size), _dtype(q), _stream(stream))
+    _check(st, "pa_varlen_attention_static_scratch")
+    return out

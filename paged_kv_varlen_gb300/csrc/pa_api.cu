@@ -124,6 +124,11 @@ SplitLayout split_layout(int num_seqs, int max_parts, int num_q_heads, int head_
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 }  // namespace
+
+// Lets other translation units of the library report a message through
+// pa_last_error_string().
+void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
 }  // namespace pa
 
 using namespace pa;

@@ -74,6 +74,9 @@ __host__ __device__ constexpr int decode_tile_keys(int elem_bytes, int head_dim)
 // that a box never crosses a page boundary.
 __host__ __device__ constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
 
+// Message returned by pa_last_error_string() on this thread.
+void set_last_error(const char *msg);
+
 cudaError_t launch_reduce(int elem_bytes, int head_dim, const ReduceArgs &a, cudaStream_t stream);
 
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t stride_bytes,
