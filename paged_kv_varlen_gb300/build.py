@@ -57,10 +57,11 @@ def build_library(force: bool = False, jobs: int | None = None, verbose: bool = 
     objs = [os.path.join(BUILD_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
     todo = [(s, o) for s, o in zip(srcs, objs) if force or _stale(o, [s] + headers)]
     cc = nvcc()
+    extra = os.environ.get("PA_NVCC_EXTRA", "").split()   # e.g. tile-shape -D overrides
 
     def compile_one(so):
         src, obj = so
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj + ".tmp"]
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj + ".tmp"]
         if verbose:
             print(" ".join(cmd), flush=True)
         res = subprocess.run(cmd, capture_output=True, text=True)

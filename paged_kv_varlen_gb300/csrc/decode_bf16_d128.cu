@@ -1,4 +1,4 @@
-// Instantiation of the paged decode kernel for bf16 K/V with head_dim 128
+// Instantiations of the paged decode kernels for bf16 K/V with head_dim 128
 // (query-head groups 1..8); see decode_kernel.cuh.
 #include "decode_kernel.cuh"
 
@@ -8,5 +8,6 @@ cudaError_t launch_decode_bf16_d128(int group, const CUtensorMap &kmap, const CU
                                    const DecodeArgs &a, dim3 grid, cudaStream_t stream) {
     return launch_decode_group<__nv_bfloat16, 128>(group, kmap, vmap, a, grid, stream);
 }
+
 
 }  // namespace pa

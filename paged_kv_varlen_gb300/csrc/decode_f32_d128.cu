@@ -1,4 +1,4 @@
-// Instantiation of the paged decode kernel for f32 K/V with head_dim 128
+// Instantiations of the paged decode kernels for f32 K/V with head_dim 128
 // (query-head groups 1..8); see decode_kernel.cuh.
 #include "decode_kernel.cuh"
 
@@ -8,5 +8,6 @@ cudaError_t launch_decode_f32_d128(int group, const CUtensorMap &kmap, const CUt
                                    const DecodeArgs &a, dim3 grid, cudaStream_t stream) {
     return launch_decode_group<float, 128>(group, kmap, vmap, a, grid, stream);
 }
+
 
 }  // namespace pa

@@ -44,29 +44,35 @@ struct DecodeCfg {
     static constexpr int CPL = CPR / LPR;                     // chunks per lane (PV)
     static constexpr int NW = 4;                              // consumer warps
     static constexpr int THREADS = (NW + 1) * 32;
+    // CTAs per SM the register budget is sized for: large head groups keep more
+    // accumulators live and get a larger share of the register file.
+    static constexpr int MIN_CTAS = G <= 5 ? 3 : 2;
     static constexpr int GP = (G + 3) & ~3;                   // padded head count
     static constexpr int TILE_BYTES = TK * D * E;             // K (or V) bytes per tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    // Ring depth: a multiple of NW so that stage s always belongs to warp s % NW
-    // (tile t -> warp t % NW, stage t % NS).  Each stage then has one consumer
-    // that waits on its phases strictly in order, which the parity-based
-    // mbarrier wait requires (a waiter two phases ahead would pass early).
-    static constexpr int NS_PER_WARP = (65536 / STAGE_BYTES) / NW < 1 ? 1 : (65536 / STAGE_BYTES) / NW;
-    static constexpr int NS = NW * NS_PER_WARP;
+    // Ring depth: NSW stages per consumer warp, tile t -> warp t % NW, stage
+    // t % NS.  Stage s then always belongs to warp s % NW and has a single
+    // consumer that waits on its phases strictly in order, which the
+    // parity-based mbarrier wait requires (a waiter two phases ahead would pass
+    // early).  Two stages per warp let a warp compute on one tile while the
+    // next is in flight.
+    static constexpr int NSW = 1;
+    static constexpr int NS = NW * NSW;
     static constexpr int OFF_Q = NS * STAGE_BYTES;
     static constexpr int OFF_P = OFF_Q + G * D * 4;
-    static constexpr int OFF_BAR = OFF_P + NW * TK * GP * 4;
+    static constexpr int OFF_BAR = OFF_P + NW * TK * GP * 8;
     static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
     static constexpr int SMEM_BYTES = OFF_FLAG + 16 + 1024;  // + alignment slack
     // merge scratch (reuses the stage ring once it has drained)
     static constexpr int MERGE_BYTES = NW * G * (D + 2) * 4;
     static_assert(MERGE_BYTES <= NS * STAGE_BYTES, "merge scratch must fit in the ring");
     static_assert(D % EPB == 0 && CPR % LPK == 0 && CPR % LPR == 0, "shape");
+    static_assert(LPK <= 4 && TK >= 8, "lane mapping needs 8..32 keys per tile");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS)
+__global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, DecodeCfg<T, D, G>::MIN_CTAS)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
     using C = DecodeCfg<T, D, G>;
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS)
         k1 = max(0, nvis);
     }
     const int ntiles = (k1 - k0 + C::TK - 1) / C::TK;
-    const int BR = gcd_int(C::TK, bs);                 // rows per TMA box
+    const int BR = a.box_rows;                         // rows per TMA box (divides TK)
     const int SUB = C::TK / BR;                        // boxes (pages) per tile per D-box
 
     // ---------------------------------------------------------------- setup
@@ -187,7 +193,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS)
                     const int row0 = page * bs + key % bs;
 #pragma unroll
                     for (int b = 0; b < C::NBOX; ++b) {
-                        const uint32_t off = (u * C::NBOX + b) * box_bytes;
+                        // stage layout [box b][key][128 B]: key rows of a box stay
+                        // consecutive, so consumers address a key without dividing
+                        const uint32_t off = (b * C::TK + u * BR) * 128;
                         tma_load_3d(sk + off, &kmap, b * C::EPB, h, row0, bar_full + 8 * s, pol);
                         tma_load_3d(sv + off, &vmap, b * C::EPB, h, row0, bar_full + 8 * s, pol);
                     }
@@ -206,22 +214,26 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS)
     }
 
     // ================================================================ consumers
+    // Packed fp32x2 arithmetic: pairs of adjacent elements share one FFMA2.
+    constexpr int HV = C::VEC / 2;                     // element pairs per 16-B chunk
     float m[G], l[G];
-    float acc[G][C::CPL * C::VEC];
+    float2 acc[G][C::CPL * HV];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         m[g] = -INFINITY;
         l[g] = 0.f;
 #pragma unroll
-        for (int e = 0; e < C::CPL * C::VEC; ++e) acc[g][e] = 0.f;
+        for (int e = 0; e < C::CPL * HV; ++e) acc[g][e] = make_float2(0.f, 0.f);
     }
     // QK lane mapping: quarter-warps share a half so one wavefront reads 8 rows
     const int qk_key = (lane & 7) + 8 * (lane / (8 * C::LPK));
     const int qk_half = (lane >> 3) % C::LPK;
-    // PV lane mapping
+    const uint32_t qk_row = qk_key * 128;
+    const int qk_x = qk_key & 7;
+    // PV lane mapping: lane owns chunk pv_lane (+ LPR * ci) of rows pv_sub + KPS*k
     const int pv_sub = lane / C::LPR;
     const int pv_lane = lane % C::LPR;
-    float *psw = ps + warp * C::TK * C::GP;
+    float2 *psw = reinterpret_cast<float2 *>(ps) + warp * C::TK * C::GP;   // (p, p) pairs
 
     for (int t = warp; t < ntiles; t += C::NW) {
         const int s = t % C::NS;
@@ -232,38 +244,34 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS)
         const uint32_t sv = sk + C::TILE_BYTES;
 
         // ---- scores t_j = <q * scale * log2e, k_j> for this lane's key
-        float sc[G];
+        float2 sc2[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) sc[g] = 0.f;
-        {
-            const int u = qk_key / BR, rw = qk_key % BR;
-            const uint32_t rowbase = sk + (u * C::NBOX * BR + rw) * 128;
+        for (int g = 0; g < G; ++g) sc2[g] = make_float2(0.f, 0.f);
 #pragma unroll 4
-            for (int i = 0; i < C::CPK; ++i) {
-                const int c = qk_half * C::CPK + i;
-                const uint32_t addr = rowbase + (c >> 3) * BR * 128 + (((c & 7) ^ (rw & 7)) << 4);
-                float kf[C::VEC];
-                Elem<T>::unpack(lds128(addr), kf);
+        for (int i = 0; i < C::CPK; ++i) {
+            const int c = qk_half * C::CPK + i;
+            const uint32_t addr = sk + (c >> 3) * (C::TK * 128) + qk_row + (((c & 7) ^ qk_x) << 4);
+            float kf[C::VEC];
+            Elem<T>::unpack(lds128(addr), kf);
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float4 *qv = reinterpret_cast<const float4 *>(qs + g * D + c * C::VEC);
+            for (int g = 0; g < G; ++g) {
+                const float4 *qv = reinterpret_cast<const float4 *>(qs + g * D + c * C::VEC);
 #pragma unroll
-                    for (int v4 = 0; v4 < C::VEC / 4; ++v4) {
-                        const float4 qq = qv[v4];
-                        sc[g] = fmaf(qq.x, kf[4 * v4 + 0], sc[g]);
-                        sc[g] = fmaf(qq.y, kf[4 * v4 + 1], sc[g]);
-                        sc[g] = fmaf(qq.z, kf[4 * v4 + 2], sc[g]);
-                        sc[g] = fmaf(qq.w, kf[4 * v4 + 3], sc[g]);
-                    }
+                for (int v4 = 0; v4 < C::VEC / 4; ++v4) {
+                    const float4 qq = qv[v4];
+                    sc2[g] = __ffma2_rn(make_float2(qq.x, qq.y),
+                                        make_float2(kf[4 * v4 + 0], kf[4 * v4 + 1]), sc2[g]);
+                    sc2[g] = __ffma2_rn(make_float2(qq.z, qq.w),
+                                        make_float2(kf[4 * v4 + 2], kf[4 * v4 + 3]), sc2[g]);
                 }
             }
         }
-        if (C::LPK > 1) {
+        float sc[G];
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], 8);
-                if (C::LPK > 2) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], 16);
-            }
+        for (int g = 0; g < G; ++g) {
+            sc[g] = sc2[g].x + sc2[g].y;
+            if (C::LPK > 1) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], 8);
+            if (C::LPK > 2) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], 16);
         }
         const bool valid = qk_key < cnt;
         // ---- one online-softmax update per tile (log2 domain)
@@ -277,39 +285,46 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS)
             const float pg = none ? 0.f : exp2f(sg - mnew);
             l[g] = l[g] * corr[g] + (qk_half == 0 ? pg : 0.f);
             m[g] = mnew;
-            if (qk_half == 0) psw[qk_key * C::GP + g] = pg;
+            if (qk_half == 0) psw[qk_key * C::GP + g] = make_float2(pg, pg);
         }
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g) {
+            const float2 cc = make_float2(corr[g], corr[g]);
 #pragma unroll
-            for (int e = 0; e < C::CPL * C::VEC; ++e) acc[g][e] *= corr[g];
+            for (int e = 0; e < C::CPL * HV; ++e) acc[g][e] = __fmul2_rn(acc[g][e], cc);
+        }
         __syncwarp();
 
         // ---- acc += p_j * v_j over the valid keys of the tile
-        for (int j = pv_sub; j < cnt; j += C::KPS) {
-            const int u = j / BR, rw = j % BR;
-            const uint32_t rowbase = sv + (u * C::NBOX * BR + rw) * 128;
-            float pj[C::GP];
+        auto pv_row = [&](int j) {
+            float2 pj[C::GP];
 #pragma unroll
-            for (int g4 = 0; g4 < C::GP / 4; ++g4) {
-                const float4 pv = reinterpret_cast<const float4 *>(psw + j * C::GP)[g4];
-                pj[4 * g4 + 0] = pv.x;
-                pj[4 * g4 + 1] = pv.y;
-                pj[4 * g4 + 2] = pv.z;
-                pj[4 * g4 + 3] = pv.w;
+            for (int g2 = 0; g2 < C::GP / 2; ++g2) {
+                const float4 pv = reinterpret_cast<const float4 *>(psw + j * C::GP)[g2];
+                pj[2 * g2 + 0] = make_float2(pv.x, pv.y);
+                pj[2 * g2 + 1] = make_float2(pv.z, pv.w);
             }
+            const uint32_t row = sv + j * 128;
+            const int jx = j & 7;
 #pragma unroll
             for (int ci = 0; ci < C::CPL; ++ci) {
                 const int c = pv_lane + ci * C::LPR;
-                const uint32_t addr = rowbase + (c >> 3) * BR * 128 + (((c & 7) ^ (rw & 7)) << 4);
+                const uint32_t addr = row + (c >> 3) * (C::TK * 128) + (((c & 7) ^ jx) << 4);
                 float vf[C::VEC];
                 Elem<T>::unpack(lds128(addr), vf);
 #pragma unroll
                 for (int g = 0; g < G; ++g)
 #pragma unroll
-                    for (int e = 0; e < C::VEC; ++e)
-                        acc[g][ci * C::VEC + e] = fmaf(pj[g], vf[e], acc[g][ci * C::VEC + e]);
+                    for (int e = 0; e < HV; ++e)
+                        acc[g][ci * HV + e] = __ffma2_rn(
+                            pj[g], make_float2(vf[2 * e], vf[2 * e + 1]), acc[g][ci * HV + e]);
             }
+        };
+        if (cnt == C::TK) {
+#pragma unroll
+            for (int jj = 0; jj < C::TK / C::KPS; ++jj) pv_row(jj * C::KPS + pv_sub);
+        } else {
+            for (int j = pv_sub; j < cnt; j += C::KPS) pv_row(j);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
@@ -322,8 +337,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS)
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
-            for (int e = 0; e < C::CPL * C::VEC; ++e)
-                acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+            for (int e = 0; e < C::CPL * HV; ++e) {
+                acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, o);
+                acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, o);
+            }
 #pragma unroll
     for (int g = 0; g < G; ++g) l[g] = warp_sum(l[g]);
 
@@ -344,9 +361,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS)
 #pragma unroll
             for (int ci = 0; ci < C::CPL; ++ci)
 #pragma unroll
-                for (int e = 0; e < C::VEC; ++e)
-                    os[(warp * G + g) * D + (pv_lane + ci * C::LPR) * C::VEC + e] =
-                        acc[g][ci * C::VEC + e];
+                for (int e = 0; e < HV; ++e) {
+                    float *o = os + (warp * G + g) * D + (pv_lane + ci * C::LPR) * C::VEC + 2 * e;
+                    o[0] = acc[g][ci * HV + e].x;
+                    o[1] = acc[g][ci * HV + e].y;
+                }
     }
     named_barrier_sync(1, C::NW * 32);
 

@@ -256,6 +256,8 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
 
     // ---- tensor maps over the two caches
     const int e = dtype == PA_F32 ? 4 : 2;
+    // TMA box height: divides the kernel's tile length and the block size, so a
+    // box never crosses a page
     const int box_rows = gcd_int(decode_tile_keys(e, head_dim), block_size);
     CUtensorMap kmap, vmap;
     st = make_cache_map(&kmap, key_cache, dtype, head_dim, num_kv_heads, num_blocks * block_size,
@@ -287,6 +289,7 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
     a.part_l = part_l;
     a.total_q = total_q;
     a.err = dev.err;
+    a.box_rows = box_rows;
 
     auto launch = [&](dim3 grid) -> cudaError_t {
         if (dtype == PA_F32) {

@@ -35,6 +35,7 @@ struct DecodeArgs {
     float *part_l;             // [num_seqs, max_parts, Hq]
     int64_t total_q;
     int *err;                  // device error word
+    int box_rows;              // rows per TMA box: divides both kernels' tile lengths
 };
 
 struct ReduceArgs {
@@ -64,10 +65,13 @@ PA_DECLARE_DECODE(launch_decode_bf16_d128)
 PA_DECLARE_DECODE(launch_decode_bf16_d256)
 #undef PA_DECLARE_DECODE
 
-// Keys per tile of the decode kernel: 32 keys for rows of up to 256 bytes
-// (one lane per key), 16 for 512-byte rows, 8 for 1024-byte rows.
+
+// Keys per tile of the decode kernel: 16 KB of K+V per tile (32 rows of
+// 256 B, 16 rows of 512 B, 8 rows of 1024 B), between 8 and 32 keys (one to
+// four lanes per key in the QK step).
 __host__ __device__ constexpr int decode_tile_keys(int elem_bytes, int head_dim) {
-    return head_dim * elem_bytes <= 256 ? 32 : (head_dim * elem_bytes == 512 ? 16 : 8);
+    return 8192 / (head_dim * elem_bytes) > 32 ? 32
+           : (8192 / (head_dim * elem_bytes) < 8 ? 8 : 8192 / (head_dim * elem_bytes));
 }
 
 // gcd of the tile length and the block size: the rows one TMA box copies, so
