@@ -103,6 +103,32 @@ pa_status make_cache_map(CUtensorMap *map, const void *cache, pa_dtype dtype, in
     return PA_OK;
 }
 
+// A 3-D map over the packed bf16 queries: x = element of a head row (D),
+// y = query head, z = packed query row.  A box is one 128-byte chunk of the
+// `group` heads of one KV head for `rows` consecutive query rows, i.e. one
+// MMA row per (query row, head), 128-byte swizzled.
+pa_status make_query_map(CUtensorMap *map, const void *q, int head_dim, int num_q_heads,
+                         int64_t total_q, int group, int rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled unavailable");
+        return PA_ERR_CUDA;
+    }
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)head_dim * num_q_heads * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled (queries) failed (%d)",
+                 (int)r);
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -148,7 +174,7 @@ PA_API const char *pa_last_error_string(void) { return g_last_error; }
 
 PA_API const char *pa_build_info(void) {
     return "libpa paged varlen attention; sm_103a; kernels: reshape_and_cache, "
-           "paged_decode (TMA ring, CUDA cores), split_reduce";
+           "paged_decode (TMA ring, CUDA cores), paged_prefill_tc (tcgen05/TMEM), split_reduce";
 }
 
 PA_API int pa_choose_partition_size(int num_seqs, int num_kv_heads, int max_seqlen_k,
@@ -310,8 +336,44 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
     a.mode = 0;
     cudaError_t ce = launch(dim3(max_parts, num_kv_heads, num_seqs));
     if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode launch");
-    // 2) rows of multi-query requests (verify windows, prefill chunks)
-    if (max_seqlen_q > 1) {
+    // 2) rows of multi-query requests (verify windows, prefill chunks): bf16 on
+    //    the tensor cores, float32 on the CUDA-core row kernel
+    if (max_seqlen_q > 1 && dtype == PA_BF16) {
+        const int bq = tc_block_rows(group);
+        const int tc_box = gcd_int(tc_tile_keys(head_dim), block_size);
+        CUtensorMap qmap, kmap_tc, vmap_tc;
+        st = make_query_map(&qmap, q, head_dim, num_q_heads, total_q, group, bq);
+        if (st != PA_OK) return st;
+        st = make_cache_map(&kmap_tc, key_cache, dtype, head_dim, num_kv_heads,
+                            num_blocks * block_size, tc_box);
+        if (st != PA_OK) return st;
+        st = make_cache_map(&vmap_tc, value_cache, dtype, head_dim, num_kv_heads,
+                            num_blocks * block_size, tc_box);
+        if (st != PA_OK) return st;
+        TcArgs ta;
+        ta.out = out;
+        ta.cu_seqlens_q = cu_seqlens_q;
+        ta.seq_lens_k = seq_lens_k;
+        ta.block_tables = block_tables;
+        ta.max_blocks_per_seq = max_blocks_per_seq;
+        ta.num_seqs = num_seqs;
+        ta.num_q_heads = num_q_heads;
+        ta.num_kv_heads = num_kv_heads;
+        ta.block_size = block_size;
+        ta.qscale = scale * kLog2e;
+        ta.sinks = sinks;
+        ta.causal = causal ? 1 : 0;
+        ta.box_rows = tc_box;
+        ta.err = dev.err;
+        // virtual query blocks: request r owns blocks cu_seqlens_q[r] / bq + r ...
+        const dim3 grid((unsigned)(total_q / bq + num_seqs), num_kv_heads, 1);
+        switch (head_dim) {
+            case 64: ce = launch_prefill_tc_d64(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
+            case 128: ce = launch_prefill_tc_d128(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
+            default: ce = launch_prefill_tc_d256(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
+        }
+        if (ce != cudaSuccess) return cuda_fail(ce, "paged_prefill_tc launch");
+    } else if (max_seqlen_q > 1) {
         a.mode = 1;
         ce = launch(dim3((unsigned)total_q, num_kv_heads, 1));
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_rows launch");

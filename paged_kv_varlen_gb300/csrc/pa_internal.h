@@ -38,6 +38,28 @@ struct DecodeArgs {
     int box_rows;              // rows per TMA box: divides both kernels' tile lengths
 };
 
+// Arguments of the tensor-core kernel for multi-query rows (bf16).
+struct TcArgs {
+    void *out;                 // [total_q, Hq, D] bf16
+    const int32_t *cu_seqlens_q;
+    const int32_t *seq_lens_k;
+    const int32_t *block_tables;
+    int max_blocks_per_seq;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int block_size;
+    float qscale;              // scale * log2(e)
+    const float *sinks;        // [Hq] or nullptr
+    int causal;
+    int box_rows;              // rows per K/V TMA box (divides the tile and the block size)
+    int *err;                  // device error word
+};
+
+// Keys per K/V tile of the tensor-core kernel and query rows per block.
+__host__ __device__ constexpr int tc_tile_keys(int head_dim) { return head_dim >= 256 ? 64 : 128; }
+__host__ __device__ constexpr int tc_block_rows(int group) { return 128 / group; }
+
 struct ReduceArgs {
     void *out;
     const float *part_o;
@@ -80,6 +102,15 @@ __host__ __device__ constexpr int gcd_int(int a, int b) { return b == 0 ? a : gc
 
 // Message returned by pa_last_error_string() on this thread.
 void set_last_error(const char *msg);
+
+// Tensor-core kernel for multi-query rows, per head_dim (bf16 only).
+#define PA_DECLARE_TC(NAME) \
+    cudaError_t NAME(int group, const CUtensorMap &qmap, const CUtensorMap &kmap, \
+                     const CUtensorMap &vmap, const TcArgs &a, dim3 grid, cudaStream_t stream);
+PA_DECLARE_TC(launch_prefill_tc_d64)
+PA_DECLARE_TC(launch_prefill_tc_d128)
+PA_DECLARE_TC(launch_prefill_tc_d256)
+#undef PA_DECLARE_TC
 
 cudaError_t launch_reduce(int elem_bytes, int head_dim, const ReduceArgs &a, cudaStream_t stream);
 

@@ -1,0 +1,421 @@
+// prefill_tc.cuh -- multi-query rows (speculative-verify windows, prefill
+// chunks) on the 5th-generation tensor cores.
+//
+// What it computes (aisignalhub.me, "packed queries and paged KV"; kwkr.cn,
+// "What is Paged Attention" and the kernel table): for the query rows of a
+// request with n > 1 rows, softmax(scale * Q K^T) V over the request's paged
+// keys, causal rows bottom-right aligned (row i sees keys j <= N - n + i),
+// with the sink logit of each head counted once in the denominator.
+//
+// GB300 design (one CTA per (request, KV head, query block), 192 threads):
+//  * An MMA row is a (query row, head) pair: BQ = 128 / G query rows times the
+//    G heads of one KV head fill M = 128, so every K/V page read serves the
+//    whole GQA group.  The grid walks virtual query blocks: request r owns
+//    blocks cu_seqlens_q[r] / BQ + r onward, found by a binary search over
+//    cu_seqlens_q; blocks are visited heaviest (last, causally) first.
+//  * Warp 4 (producer): TMA loads Q once (3-D box over [total_q, H_q, D]) and
+//    streams K/V tiles of BN keys page by page through NSTAGE stages, each a
+//    128-byte-swizzled K-major layout (the tensor cores' canonical layout).
+//  * Warp 5 (MMA): allocates 512 TMEM columns, issues S = Q K^T into one of
+//    two TMEM buffers (so QK of tile j+1 overlaps the softmax of tile j) and
+//    O += P V with V read MN-major; commits signal mbarriers.
+//  * Warps 0-3 (softmax, one thread per TMEM lane = MMA row): load S, mask and
+//    scale into the log2 domain, keep a running max with lazy rescaling of O
+//    (only when the max grows by more than 2^8), write P as bf16 into shared
+//    memory for the PV MMA, and finally normalise O from TMEM into the output.
+//  * V rows past the last key of a partial tile are zeroed before the PV MMA
+//    reads them: pool slots past the sequence may hold anything, and a
+//    zero-weight NaN would still poison the tensor-core sum.
+#pragma once
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+#include "tc_common.cuh"
+
+namespace pa {
+
+template <int D, int G>
+struct TcCfg {
+    static constexpr int BQ = 128 / G;                 // query rows per block
+    static constexpr int M_USED = BQ * G;              // MMA rows in use (<= 128)
+    static constexpr int BN = tc_tile_keys(D);         // keys per K/V tile
+    static constexpr int KCH = D / 64;                 // 128-byte chunks of a head row
+    static constexpr int Q_BYTES = KCH * 128 * 128;    // [KCH][128 rows][128 B]
+    static constexpr int KV_TILE = KCH * BN * 128;     // [KCH][BN rows][128 B]
+    static constexpr int NSTAGE = D >= 128 ? 2 : 3;
+    static constexpr int P_BYTES = (BN / 64) * 128 * 128;   // [BN/64][128 rows][128 B]
+    static constexpr int OFF_KV = Q_BYTES;
+    static constexpr int OFF_P = OFF_KV + NSTAGE * 2 * KV_TILE;
+    static constexpr int NBAR = 1 + 2 * NSTAGE + 2 + 2 + 1 + 1;
+    static constexpr int OFF_BAR = OFF_P + P_BYTES;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM base, abort flag
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int O_COL = 2 * BN;
+    static constexpr int THREADS = 192;
+    static_assert(O_COL + D <= TMEM_COLS, "TMEM columns");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(BN % 64 == 0 && D % 64 == 0, "tile shape");
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(192, 1)
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
+                            const __grid_constant__ CUtensorMap kmap,
+                            const __grid_constant__ CUtensorMap vmap, const TcArgs a) {
+    using C = TcCfg<D, G>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t q_smem = sbase;
+    const uint32_t kv_smem = sbase + C::OFF_KV;
+    const uint32_t p_smem = sbase + C::OFF_P;
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    const uint32_t bar_q = bar0;
+    const uint32_t bar_kv_full = bar0 + 8;
+    const uint32_t bar_kv_empty = bar_kv_full + 8 * C::NSTAGE;
+    const uint32_t bar_s_full = bar_kv_empty + 8 * C::NSTAGE;   // [2]
+    const uint32_t bar_s_free = bar_s_full + 16;                 // [2]
+    const uint32_t bar_p_full = bar_s_free + 16;
+    const uint32_t bar_o_done = bar_p_full + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int h = blockIdx.y;
+    const int Hq = a.num_q_heads;
+    const int bs = a.block_size;
+
+    // ---------------------------------------------------------------- work item
+    // Virtual block t belongs to the last request r with cu[r] / BQ + r <= t.
+    const int t = blockIdx.x;
+    int lo = 0, hi = a.num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.cu_seqlens_q[mid] / C::BQ + mid <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    const int r = lo;
+    const int c0 = a.cu_seqlens_q[r];
+    const int n = a.cu_seqlens_q[r + 1] - c0;
+    const int nblk = (n + C::BQ - 1) / C::BQ;
+    const int local = t - (c0 / C::BQ + r);
+    if (n <= 1 || local < 0 || local >= nblk) return;    // single-query rows: decode kernel
+    const int qb = nblk - 1 - local;                      // heaviest block first
+    const int i0 = qb * C::BQ;
+    const int rows = min(C::BQ, n - i0);
+    int N = a.seq_lens_k[r];
+    N = max(0, min(N, a.max_blocks_per_seq * bs));
+    const int kend = max(0, a.causal ? min(N, N - n + i0 + rows) : N);
+    const int ntiles = (kend + C::BN - 1) / C::BN;
+    const int64_t row_base = (int64_t)c0 + i0;
+
+    // ---------------------------------------------------------------- setup
+    if (tid == 0) {
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < C::NSTAGE; ++s) {
+            mbar_init(bar_kv_full + 8 * s, 1);
+            mbar_init(bar_kv_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_s_full + 8 * b, 1);
+            mbar_init(bar_s_free + 8 * b, 4);
+        }
+        mbar_init(bar_p_full, 4);
+        mbar_init(bar_o_done, 1);
+        fence_barrier_init();
+        *abort_flag = 0;
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ============================================================ producer
+        const int BR = a.box_rows;
+        const int SUB = C::BN / BR;
+        const uint64_t pol_kv = policy_evict_last();   // K/V are re-read by other query blocks
+        if (lane == 0) {
+            prefetch_tensormap(&qmap);
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+            mbar_arrive_expect_tx(bar_q, C::KCH * C::M_USED * 128);
+            const uint64_t pol_q = policy_evict_first();
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+                tma_load_3d(q_smem + c * 128 * 128, &qmap, c * 64, h * G, (int)row_base, bar_q,
+                            pol_q);
+        }
+        const int32_t *bt = a.block_tables + (int64_t)r * a.max_blocks_per_seq;
+        const int nsb_total = (kend + BR - 1) / BR;
+        auto page_of = [&](int gsb) -> int { return gsb < nsb_total ? bt[(gsb * BR) / bs] : 0; };
+        int base = 0;
+        int cur = page_of(lane);
+        int nxt = page_of(32 + lane);
+        int issued = 0;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j % C::NSTAGE;
+            const int use = j / C::NSTAGE;
+            int bad = 0;
+            if (lane == 0 && use > 0)
+                bad = !mbar_wait(bar_kv_empty + 8 * st, (use - 1) & 1, a.err, abort_flag);
+            if (__shfl_sync(0xffffffffu, bad, 0)) break;
+            const int cnt = min(C::BN, kend - j * C::BN);
+            const int nsub = (cnt + BR - 1) / BR;
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar_kv_full + 8 * st, nsub * C::KCH * BR * 128 * 2);
+            __syncwarp();
+            const uint32_t ks = kv_smem + st * 2 * C::KV_TILE;
+            const uint32_t vs = ks + C::KV_TILE;
+            for (int u = 0; u < nsub; ++u) {
+                const int gsb = j * SUB + u;
+                if (gsb >= base + 32) {
+                    base += 32;
+                    cur = nxt;
+                    nxt = page_of(base + 32 + lane);
+                }
+                const int page = __shfl_sync(0xffffffffu, cur, gsb - base);
+                if (lane == 0) {
+                    const int row0 = page * bs + (gsb * BR) % bs;
+#pragma unroll
+                    for (int c = 0; c < C::KCH; ++c) {
+                        const uint32_t off = c * C::BN * 128 + u * BR * 128;
+                        tma_load_3d(ks + off, &kmap, c * 64, h, row0, bar_kv_full + 8 * st, pol_kv);
+                        tma_load_3d(vs + off, &vmap, c * 64, h, row0, bar_kv_full + 8 * st, pol_kv);
+                    }
+                }
+            }
+            __syncwarp();
+            issued = j + 1;
+        }
+        if (lane == 0) {
+            mbar_drain(bar_q, 0, kWaitLimitCycles / 8);
+            for (int j = max(0, issued - C::NSTAGE); j < issued; ++j)
+                mbar_drain(bar_kv_full + 8 * (j % C::NSTAGE), (j / C::NSTAGE) & 1,
+                           kWaitLimitCycles / 8);
+        }
+    } else if (warp == 5) {
+        // ============================================================ MMA issuer
+        if (lane == 0 && ntiles > 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16_f32(128, C::BN, 0, 0);
+            constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
+            mbar_wait(bar_q, 0, a.err, abort_flag);
+            auto issue_pv = [&](int jj) {
+                mbar_wait(bar_p_full, jj & 1, a.err, abort_flag);
+                tc_fence_after();
+                const int stp = jj % C::NSTAGE;
+                const uint32_t vs = kv_smem + stp * 2 * C::KV_TILE + C::KV_TILE;
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk) {
+                    const uint64_t ad =
+                        smem_desc_sw128(p_smem + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(vs + kk * 16 * 128, C::BN * 128, 1024);
+                    tc_mma_bf16(tmem + C::O_COL, ad, bd, IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar_o_done);
+                tc_commit(bar_kv_empty + 8 * stp);
+            };
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j % C::NSTAGE;
+                const int sb = j & 1;
+                mbar_wait(bar_kv_full + 8 * st, (j / C::NSTAGE) & 1, a.err, abort_flag);
+                if (j >= 2) mbar_wait(bar_s_free + 8 * sb, ((j >> 1) - 1) & 1, a.err, abort_flag);
+                tc_fence_after();
+                const uint32_t ks = kv_smem + st * 2 * C::KV_TILE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;   // 16 bf16 within the 128-B row
+                    const uint64_t ad =
+                        smem_desc_sw128(q_smem + (kk >> 2) * 128 * 128 + off, 16, 1024);
+                    const uint64_t bd =
+                        smem_desc_sw128(ks + (kk >> 2) * C::BN * 128 + off, 16, 1024);
+                    tc_mma_bf16(tmem + sb * C::BN, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar_s_full + 8 * sb);
+                if (j >= 1) issue_pv(j - 1);
+            }
+            issue_pv(ntiles - 1);
+            // every MMA must be finished before TMEM is freed (bounded wait that
+            // also holds on an aborted pipeline)
+            mbar_drain(bar_o_done, (ntiles - 1) & 1, kWaitLimitCycles / 8);
+        }
+    } else {
+        // ============================================================ softmax
+        const int m = tid;                                // MMA row = TMEM lane
+        const int i = m / G, g = m % G;
+        const bool row_ok = (m < C::M_USED) && (i < rows);
+        const int qi = i0 + i;
+        const int lim = min(N - 1, a.causal ? N - n + qi : N - 1);   // last visible key
+        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
+        for (int j = 0; j < ntiles; ++j) {
+            const int sb = j & 1;
+            const int st = j % C::NSTAGE;
+            mbar_wait(bar_s_full + 8 * sb, (j >> 1) & 1, a.err, abort_flag);
+            tc_fence_after();
+            float s[C::BN];
+#pragma unroll
+            for (int c = 0; c < C::BN / 32; ++c) tmem_ld32(t_lane + sb * C::BN + 32 * c, s + 32 * c);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_s_free + 8 * sb);
+
+            const int kt0 = j * C::BN;
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < C::BN; ++c) {
+                const bool vis = row_ok && (kt0 + c <= lim);
+                s[c] = vis ? s[c] * a.qscale : -INFINITY;
+                tmax = fmaxf(tmax, s[c]);
+            }
+            const float m_new = fmaxf(m_run, tmax);
+            m_run = m_new;
+            const bool need = (m_new != -INFINITY) && (m_ref == -INFINITY || m_new > m_ref + 8.f);
+
+            // Value rows past the tile's last key may hold anything: zero them
+            // before the PV MMA (a zero weight times NaN is still NaN).
+            const int cnt = min(C::BN, kend - kt0);
+            if (cnt < C::BN) {
+                mbar_wait(bar_kv_full + 8 * st, (j / C::NSTAGE) & 1, a.err, abort_flag);
+                uint8_t *vsp = smem + C::OFF_KV + st * 2 * C::KV_TILE + C::KV_TILE;
+                const int nchunk = (C::BN - cnt) * 8;     // 16-byte chunks per D-chunk region
+                for (int c = 0; c < C::KCH; ++c)
+                    for (int q = tid; q < nchunk; q += 128)
+                        *reinterpret_cast<uint4 *>(vsp + c * C::BN * 128 + cnt * 128 + q * 16) =
+                            make_uint4(0, 0, 0, 0);
+            }
+            // PV of the previous tile must be done before O or the P buffer change.
+            if (j >= 1) {
+                mbar_wait(bar_o_done, (j - 1) & 1, a.err, abort_flag);
+                tc_fence_after();
+            }
+            if (j >= 1 && __any_sync(0xffffffffu, need)) {
+                const float f = need ? (m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new)) : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(t_lane + C::O_COL + 32 * c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= f;
+                    tmem_st32(t_lane + C::O_COL + 32 * c, o);
+                }
+                tmem_wait_st();
+            }
+            if (need) {
+                l *= (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
+                m_ref = m_new;
+            }
+            // P = 2^(s - m_ref) as bf16, row m of the K-major 128-byte-swizzled A tile
+#pragma unroll
+            for (int k8 = 0; k8 < C::BN / 8; ++k8) {
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float x = s[k8 * 8 + e];
+                    p[e] = (x == -INFINITY) ? 0.f : exp2f(x - m_ref);
+                    l += p[e];
+                }
+                const uint32_t addr = p_smem + (k8 >> 3) * 128 * 128 + m * 128 +
+                                      (((k8 & 7) ^ (m & 7)) << 4);
+                sts128(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                       pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_p_full);
+        }
+        // ---- epilogue: out = O / (l + sink term)
+        if (ntiles > 0) {
+            mbar_wait(bar_o_done, (ntiles - 1) & 1, a.err, abort_flag);
+            tc_fence_after();
+        }
+        float scale_out = 0.f;
+        if (l > 0.f) {
+            if (a.sinks) {
+                const float sk2 = a.sinks[h * G + g] * kLog2e;
+                const float M2 = fmaxf(m_ref, sk2);
+                const float f = exp2f(m_ref - M2);
+                scale_out = f / (l * f + exp2f(sk2 - M2));
+            } else {
+                scale_out = 1.f / l;
+            }
+        }
+        __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(a.out) +
+                              ((row_base + i) * Hq + (int64_t)h * G + g) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            if (ntiles > 0) {
+                tmem_ld32(t_lane + C::O_COL + 32 * c, o);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = 0.f;
+            }
+            if (row_ok) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(pack_bf16x2(o[8 * q + 0] * scale_out, o[8 * q + 1] * scale_out),
+                                        pack_bf16x2(o[8 * q + 2] * scale_out, o[8 * q + 3] * scale_out),
+                                        pack_bf16x2(o[8 * q + 4] * scale_out, o[8 * q + 5] * scale_out),
+                                        pack_bf16x2(o[8 * q + 6] * scale_out, o[8 * q + 7] * scale_out));
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D, int G>
+cudaError_t launch_prefill_tc_t(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                                const CUtensorMap &vmap, const TcArgs &a, dim3 grid,
+                                cudaStream_t stream) {
+    using C = TcCfg<D, G>;
+    auto kern = paged_prefill_tc_kernel<D, G>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qmap, kmap, vmap, a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_prefill_tc_group(int group, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                                    const CUtensorMap &vmap, const TcArgs &a, dim3 grid,
+                                    cudaStream_t stream) {
+    switch (group) {
+        case 1: return launch_prefill_tc_t<D, 1>(qmap, kmap, vmap, a, grid, stream);
+        case 2: return launch_prefill_tc_t<D, 2>(qmap, kmap, vmap, a, grid, stream);
+        case 3: return launch_prefill_tc_t<D, 3>(qmap, kmap, vmap, a, grid, stream);
+        case 4: return launch_prefill_tc_t<D, 4>(qmap, kmap, vmap, a, grid, stream);
+        case 5: return launch_prefill_tc_t<D, 5>(qmap, kmap, vmap, a, grid, stream);
+        case 6: return launch_prefill_tc_t<D, 6>(qmap, kmap, vmap, a, grid, stream);
+        case 7: return launch_prefill_tc_t<D, 7>(qmap, kmap, vmap, a, grid, stream);
+        case 8: return launch_prefill_tc_t<D, 8>(qmap, kmap, vmap, a, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pa
