@@ -2,29 +2,36 @@
 
 One step = one pass of the whole hot path over one batch: the KV scatter of
 this step's tokens (pa_reshape_and_cache), then attention over the packed
-query rows and paged K/V (pa_varlen_attention: split-KV decode kernel + the
-shared reduce).  Default workload: the GQA decode batch -- 32 requests with
-contexts U[512, 8192], (H_q, H_kv, D) = (32, 8, 128), bf16, block size 16,
-40k-page shuffled pool, split-KV partition 512.
+query rows and paged K/V (pa_varlen_attention: the split-KV decode kernel and
+its shared reduce for single-query rows, the tcgen05 kernel for multi-query
+rows).
 
-Metric: decode KV GB/s = algorithmic bytes per step (each context token's K
-and V rows once per KV head, queries, outputs, block tables, the scatter's
-reads and writes) / step time.  The accessed KV (~570 MB) exceeds the 126 MB
-L2, so no flush is needed between steps.
+Default workload (the one the headline metric is quoted on): the GQA decode
+batch -- 32 requests with contexts U[512, 8192], (H_q, H_kv, D) = (32, 8, 128),
+bf16, block size 16, 40k-page shuffled pool, split-KV partition 512.  Metric:
+decode KV GB/s = algorithmic bytes per step / step time.  ``--workload`` picks
+another seeded workload (2: varlen causal prefill -> TFLOP/s; 3: mixed packed
+step -> tokens/s; 4: long-context decode with sinks -> GB/s).
+
+Algorithmic work per step: every visible (query row, key) pair costs
+4 * D flops per query head (QK^T and PV); bytes are each context token's K and
+V rows once per KV head, the queries and outputs, the block tables and the
+scatter's reads and writes.  The accessed KV exceeds the 126 MB L2 on the decode
+workloads, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1..4] [--no-cpu-baseline]
 
 Under torchrun (N > 1) every rank runs its own independent batch (requests are
 independent units: weak scaling, no collective on the data path); timing is
-the max over ranks.  ``--impl reference`` times the fp64 CPU oracle on the
-host cores (rank 0 only) on a bounded per-step sample of the same workload.
+the max over ranks.  ``--impl reference`` times the fp64 CPU oracle on the host
+cores (rank 0 only) on a bounded per-step sample of the same workload.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -39,29 +46,28 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode paged-attn KV GB/s (% HBM peak); varlen prefill TFLOP/s; tokens/s"
-WORKLOAD_INDEX = 1
+DEFAULT_WORKLOAD = 1
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum per attention call (decode kernel
-# + reduce) from an ncu capture, valid only for the kernel sources whose hash
-# is recorded beside it; null otherwise.
+# dram__bytes_read.sum + dram__bytes_write.sum per attention call from an ncu
+# capture, valid only for the kernel sources whose hash is recorded beside it.
 NCU_TRAFFIC = {"sources_sha256": None, "bytes_per_launch": None}
 
 
 def kernel_sources_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_varlen_gb300", "csrc")
-    for f in ("decode_kernel.cuh", "pa_common.cuh", "reduce.cu"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()
 
 
 def dist_env():
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return rank, world, local
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
 def max_over_ranks(value: float, world: int, device=None) -> float:
@@ -75,15 +81,44 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def algorithmic_bytes(w) -> dict:
-    """Bytes one step must move at minimum (per the layouts of the ABI)."""
+# ------------------------------------------------------------------ algorithmic work
+def visible_keys(w) -> np.ndarray:
+    """Keys each packed query row sees (bottom-right causal alignment)."""
+    vis = np.empty(w.total_q, dtype=np.int64)
+    for r in range(w.num_seqs):
+        n, N = int(w.q_lens[r]), int(w.seq_lens[r])
+        c0 = int(w.cu_seqlens_q[r])
+        i = np.arange(n)
+        vis[c0:c0 + n] = np.clip(N - n + i + 1, 0, N) if w.causal else N
+    return vis
+
+
+def algorithmic_work(w) -> dict:
     e = 2 if w.dtype == "bf16" else 4
     kv = w.kv_bytes_read()
     qo = 2 * w.total_q * w.num_q_heads * w.head_dim * e
     pages = int(((w.seq_lens + w.block_size - 1) // w.block_size).sum())
     meta = 4 * pages + 4 * (w.num_seqs * 2 + 1)
     scatter = 2 * 2 * w.total_q * w.num_kv_heads * w.head_dim * e + 8 * w.total_q
-    return {"kv": kv, "attention": kv + qo + meta, "step": kv + qo + meta + scatter}
+    flops = 4.0 * w.head_dim * w.num_q_heads * float(visible_keys(w).sum())
+    return {"kv": kv, "attention_bytes": kv + qo + meta, "step_bytes": kv + qo + meta + scatter,
+            "flops": flops, "tokens": w.total_q}
+
+
+def workload_kind(w) -> str:
+    if w.max_seqlen_q <= 1:
+        return "decode"
+    if int((w.q_lens == 1).sum()) == 0:
+        return "prefill"
+    return "mixed"
+
+
+def metric_value(kind: str, work: dict, seconds: float, world: int):
+    if kind == "decode":
+        return world * work["step_bytes"] / seconds / 1e9, "GB/s"
+    if kind == "prefill":
+        return world * work["flops"] / seconds / 1e12, "TFLOP/s"
+    return world * work["tokens"] / seconds, "tokens/s"
 
 
 def measured_peaks():
@@ -91,9 +126,9 @@ def measured_peaks():
     try:
         with open(path) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 class ClockSampler:
@@ -115,8 +150,7 @@ class ClockSampler:
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "50", "-i", self.gpu_id], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
-            self.reader = threading.Thread(target=self._read, daemon=True)
-            self.reader.start()
+            threading.Thread(target=self._read, daemon=True).start()
         except Exception:
             self.proc = None
 
@@ -155,10 +189,8 @@ class ClockSampler:
             for name, val in zip(names, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
 
 
 def gpu_id_for(torch, device) -> str:
@@ -171,9 +203,16 @@ def gpu_id_for(torch, device) -> str:
 
 
 # ------------------------------------------------------------------ CPU oracle
+def prepare_oracle_pool(w):
+    from oracle import oracle as orc
+    w._kc_ref, w._vc_ref = orc.reshape_and_cache(w.new_k, w.new_v, w.key_cache, w.value_cache,
+                                                 w.slot_mapping, w.block_size)
+    w._vis = visible_keys(w)
+
+
 def time_oracle(w, rows, nthreads):
-    """Wall time of the fp64 oracle on the given decode rows (pool already
-    holding this step's tokens)."""
+    """Wall time of the fp64 oracle on the given query rows (pool holding this
+    step's tokens)."""
     from oracle import oracle as orc
     t0 = time.perf_counter()
     orc.paged_attention(w.q, w._kc_ref, w._vc_ref, w.cu_seqlens_q, w.seq_lens_k, w.block_tables,
@@ -183,35 +222,40 @@ def time_oracle(w, rows, nthreads):
     return time.perf_counter() - t0
 
 
-def row_bytes(w, rows):
+def rows_work(w, rows) -> dict:
+    """Work the oracle does for these rows, in the units of the GPU metric."""
     e = 2 if w.dtype == "bf16" else 4
-    total = 0
-    for row in rows:
-        r = int(np.searchsorted(w.cu_seqlens_q, row, side="right") - 1)
-        total += int(w.seq_lens_k[r]) * w.num_kv_heads * w.head_dim * e * 2
-        total += 2 * w.num_q_heads * w.head_dim * e
-    return total
+    vis = w._vis[np.asarray(rows)]
+    return {"step_bytes": float(vis.sum()) * w.num_kv_heads * w.head_dim * e * 2
+                          + len(rows) * 2 * w.num_q_heads * w.head_dim * e,
+            "flops": 4.0 * w.head_dim * w.num_q_heads * float(vis.sum()),
+            "tokens": len(rows)}
 
 
-def prepare_oracle_pool(w):
-    from oracle import oracle as orc
-    w._kc_ref, w._vc_ref = orc.reshape_and_cache(w.new_k, w.new_v, w.key_cache, w.value_cache,
-                                                 w.slot_mapping, w.block_size)
+def sample_rows(w, target_flops: float, seed: int = 0):
+    """Rows whose oracle work is about `target_flops` (all rows if less)."""
+    total = 4.0 * w.head_dim * w.num_q_heads * float(w._vis.sum())
+    if total <= target_flops:
+        return np.arange(w.total_q)
+    rng = np.random.default_rng(seed)
+    k = max(1, int(w.total_q * target_flops / total))
+    return np.sort(rng.choice(w.total_q, size=k, replace=False))
 
 
-def cpu_baseline(w, budget_s=12.0):
-    """The oracle as it stands on all host cores, on whole batches of the
-    workload until about `budget_s` of CPU work."""
+def cpu_baseline(w, kind, budget_s=12.0):
+    """The oracle as it stands on all host cores, on samples of the workload's
+    rows until about `budget_s` of CPU work."""
     nthreads = os.cpu_count() or 1
     prepare_oracle_pool(w)
-    rows = np.arange(w.total_q)
+    rows = sample_rows(w, 4e9)
     t, n = 0.0, 0
     while t < budget_s and n < 1000:
         t += time_oracle(w, rows, nthreads)
         n += 1
-    gbs = n * row_bytes(w, rows) / t / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
-            "sample": f"{n} full batch(es) of the workload ({w.total_q} decode rows, all heads), "
+    work = {k: v * n for k, v in rows_work(w, rows).items()}
+    value, unit = metric_value(kind, work, t, 1)
+    return {"value": round(value, 6), "unit": unit, "cores": nthreads, "kind": "oracle",
+            "sample": f"{n} pass(es) over {len(rows)} of {w.total_q} query rows (all heads), "
                       f"fp64 C oracle, {t:.1f} s wall"}
 
 
@@ -219,31 +263,33 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     from paged_kv_varlen_gb300 import workloads as wl
-    w = wl.workload(WORKLOAD_INDEX)
+    w = wl.workload(args.workload)
+    kind = workload_kind(w)
     prepare_oracle_pool(w)
     nthreads = os.cpu_count() or 1
-    # per-step sample: one decode row (all heads), cycling over the batch
-    order = np.arange(w.total_q)
+    # per-step sample: one query row (all heads), cycling over the batch
+    order = np.random.default_rng(1).permutation(w.total_q)
+    pick = lambda i: order[i % len(order):i % len(order) + 1]  # noqa: E731
     for i in range(args.warmup):
-        time_oracle(w, order[i % len(order):i % len(order) + 1], nthreads)
-    t_total, b_total = 0.0, 0
+        time_oracle(w, pick(i), nthreads)
+    t_total = 0.0
+    work = {"step_bytes": 0.0, "flops": 0.0, "tokens": 0}
     for i in range(args.steps):
-        rows = order[i % len(order):i % len(order) + 1]
+        rows = pick(i)
         t_total += time_oracle(w, rows, nthreads)
-        b_total += row_bytes(w, rows)
-    value = b_total / t_total / 1e9
+        for k, v in rows_work(w, rows).items():
+            work[k] += v
+    value, unit = metric_value(kind, work, t_total, 1)
+    sample = "one query row (all heads) per step, cycling over the batch; fp64 C oracle"
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * t_total / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.WORKLOAD_NAMES[WORKLOAD_INDEX],
-                   "sample": "one decode row (all 32 query heads) per step"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads,
-                         "kind": "oracle",
-                         "sample": "one decode row (all heads) per step, cycling over the "
-                                   "32-row batch; fp64 C oracle"},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "config": {"workload": wl.WORKLOAD_NAMES[args.workload], "sample": sample},
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": nthreads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -262,8 +308,9 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
 
-    w = wl.workload(WORKLOAD_INDEX)
-    nbytes = algorithmic_bytes(w)
+    w = wl.workload(args.workload)
+    kind = workload_kind(w)
+    work = algorithmic_work(w)
 
     def dev(a):
         if w.dtype == "bf16":
@@ -277,6 +324,7 @@ def run_ours(args, rank, world, local):
     cu = torch.from_numpy(w.cu_seqlens_q).to(device)
     sl = torch.from_numpy(w.seq_lens_k).to(device)
     bt = torch.from_numpy(w.block_tables).to(device)
+    sk = torch.from_numpy(w.sinks).to(device) if w.sinks is not None else None
     out = torch.empty_like(q)
     P = w.partition_size
     ws_bytes = pa.pa_varlen_attention_workspace_size(w.num_seqs, w.max_seqlen_k, w.num_q_heads,
@@ -293,7 +341,7 @@ def run_ours(args, rank, world, local):
     def attend(q_in=q, cu_in=cu, sl_in=sl, bt_in=bt, o=out):
         pa.pa_varlen_attention(o, q_in, kc, vc, cu_in, sl_in, bt_in,
                                max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k,
-                               scale=w.scale, sinks=None, causal=w.causal, partition_size=P,
+                               scale=w.scale, sinks=sk, causal=w.causal, partition_size=P,
                                workspace=ws, stream=stream)
 
     def barrier():
@@ -301,12 +349,13 @@ def run_ours(args, rank, world, local):
             import torch.distributed as dist
             dist.barrier()
 
+    steps = args.steps
     # ---------------- device-resident timing
     for _ in range(args.warmup):
         scatter()
         attend()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(gpu_id_for(torch, local))
     clocks.start()
@@ -315,7 +364,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     clocks.mark_on()
     start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         ev[i][0].record(stream)
         scatter()
         ev[i][1].record(stream)
@@ -329,10 +378,10 @@ def run_ours(args, rank, world, local):
     clk = clocks.stop()
     assert pa.pa_device_error() == 0, "device error word set during the benchmark"
     elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, device)
-    attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
     attn_avg_s = max_over_ranks(sum(attn_ms) / len(attn_ms) / 1e3, world, device)
-    step_s = elapsed_s / args.steps
-    value = world * nbytes["step"] / step_s / 1e9
+    step_s = elapsed_s / steps
+    value, unit = metric_value(kind, work, step_s, world)
 
     # ---------------- end to end through the public API with host buffers
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
@@ -358,44 +407,62 @@ def run_ours(args, rank, world, local):
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         e2e_step()
     e1.record(stream)
     e1.synchronize()
     barrier()
-    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device) / args.steps
-    e2e_value = world * nbytes["step"] / e2e_s / 1e9
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device) / steps
+    e2e_value, _ = metric_value(kind, work, e2e_s, world)
 
-    # ---------------- roofline of the dominant launch (decode kernel + reduce)
-    peak, peak_kind = measured_peaks()
-    achieved = nbytes["attention"] / attn_avg_s / 1e9
-    traffic = None
-    if NCU_TRAFFIC["sources_sha256"] == kernel_sources_hash():
-        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    # ---------------- roofline of the dominant launch (the attention call)
+    hbm, bf16, peak_kind = measured_peaks()
+    t_bw = work["attention_bytes"] / (hbm * 1e9)
+    t_fl = work["flops"] / (bf16 * 1e12)
+    traffic = (NCU_TRAFFIC["bytes_per_launch"]
+               if NCU_TRAFFIC["sources_sha256"] == kernel_sources_hash() else None)
+    if kind == "decode" or (kind == "mixed" and t_bw >= t_fl):
+        roof = {"bound": "hbm", "achieved": round(work["attention_bytes"] / attn_avg_s / 1e9, 2),
+                "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": round(work["flops"] / attn_avg_s / 1e12, 2),
+                "peak": bf16, "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = traffic
+    roof["kernel"] = {"decode": "paged_decode_kernel + split_reduce_kernel",
+                      "prefill": "paged_prefill_tc_kernel",
+                      "mixed": "paged_decode_kernel + paged_prefill_tc_kernel + split_reduce_kernel"
+                      }[kind] + " (one attention call)"
+    roof["peak_source"] = (f"{peak_kind} (MEASURED_PEAKS.json "
+                           f"{'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops'})"
+                           if peak_kind == "measured" else "fallback")
+    roof["avg_launch_us"] = round(attn_avg_s * 1e6, 3)
+    if kind == "mixed":
+        roof["roofline_time_us"] = round(1e6 * max(t_bw, t_fl), 2)
+        roof["frac_of_max_roofline"] = round(max(t_bw, t_fl) / attn_avg_s, 4)
 
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * step_s, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) Q/K/V, bf16)",
-        "config": {"workload": wl.WORKLOAD_NAMES[WORKLOAD_INDEX], "num_seqs": w.num_seqs,
-                   "total_kv_tokens": int(w.seq_lens.sum()), "partition_size": P_used,
-                   "l2": "inputs larger than L2 (~570 MB of KV per step vs 126 MB L2); no flush",
+        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(1e3 * step_s, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) Q/K/V)",
+        "config": {"workload": wl.WORKLOAD_NAMES[args.workload], "num_seqs": w.num_seqs,
+                   "total_q": w.total_q, "total_kv_tokens": int(w.seq_lens.sum()),
+                   "partition_size": P_used,
+                   "l2": "no flush: the KV read per step exceeds the 126 MB L2"
+                         if work["kv"] > 2 * 126e6 else "no flush (KV partly L2-resident)",
                    "parallelism": f"independent batch per GPU x{world}"},
+        "kv_gbs": round(world * work["step_bytes"] / step_s / 1e9, 2),
+        "tflops": round(world * work["flops"] / step_s / 1e12, 3),
         "tokens_per_s": round(world * w.total_q / step_s, 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "paged_decode_kernel + split_reduce_kernel (one attention call)",
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                                    if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "avg_launch_us": round(attn_avg_s * 1e6, 3)},
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(1e3 * e2e_s, 5)},
-        "gpu_launches": int(launches_per_step * args.steps),
+        "gpu_launches": int(launches_per_step * steps),
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, kind)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -410,6 +477,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, choices=[1, 2, 3, 4], default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

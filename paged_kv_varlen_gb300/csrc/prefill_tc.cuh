@@ -7,22 +7,26 @@
 // keys, causal rows bottom-right aligned (row i sees keys j <= N - n + i),
 // with the sink logit of each head counted once in the denominator.
 //
-// GB300 design (one CTA per (request, KV head, query block), 192 threads):
+// GB300 design (one CTA per (request, KV head, query block), 224 threads):
 //  * An MMA row is a (query row, head) pair: BQ = 128 / G query rows times the
 //    G heads of one KV head fill M = 128, so every K/V page read serves the
 //    whole GQA group.  The grid walks virtual query blocks: request r owns
 //    blocks cu_seqlens_q[r] / BQ + r onward, found by a binary search over
 //    cu_seqlens_q; blocks are visited heaviest (last, causally) first.
-//  * Warp 4 (producer): TMA loads Q once (3-D box over [total_q, H_q, D]) and
-//    streams K/V tiles of BN keys page by page through NSTAGE stages, each a
-//    128-byte-swizzled K-major layout (the tensor cores' canonical layout).
+//  * Warps 4 and 6 (producers): TMA loads Q once (3-D box over [total_q, H_q,
+//    D]) and streams the K and the V tiles of BN keys page by page through
+//    separate stage rings, 128-byte-swizzled (the tensor cores' canonical
+//    layout); a K stage is released as soon as its QK^T is done, so the next
+//    K tiles load while the softmax and PV of earlier tiles run.
 //  * Warp 5 (MMA): allocates 512 TMEM columns, issues S = Q K^T into one of
 //    two TMEM buffers (so QK of tile j+1 overlaps the softmax of tile j) and
 //    O += P V with V read MN-major; commits signal mbarriers.
 //  * Warps 0-3 (softmax, one thread per TMEM lane = MMA row): load S, mask and
 //    scale into the log2 domain, keep a running max with lazy rescaling of O
-//    (only when the max grows by more than 2^8), write P as bf16 into shared
-//    memory for the PV MMA, and finally normalise O from TMEM into the output.
+//    (only when the max grows by more than 2^8), write P as bf16 into one of
+//    two shared-memory buffers for the PV MMA, and finally normalise O from
+//    TMEM into the output.  The softmax waits for a PV only to reuse its P
+//    buffer (two tiles back) or to rescale O, so softmax and MMAs overlap.
 //  * V rows past the last key of a partial tile are zeroed before the PV MMA
 //    reads them: pool slots past the sequence may hold anything, and a
 //    zero-weight NaN would still poison the tensor-core sum.
@@ -42,24 +46,25 @@ struct TcCfg {
     static constexpr int KCH = D / 64;                 // 128-byte chunks of a head row
     static constexpr int Q_BYTES = KCH * 128 * 128;    // [KCH][128 rows][128 B]
     static constexpr int KV_TILE = KCH * BN * 128;     // [KCH][BN rows][128 B]
-    static constexpr int NSTAGE = D >= 128 ? 2 : 3;
+    static constexpr int NSTAGE = D >= 128 ? 2 : 3;    // K stages (and as many V stages)
     static constexpr int P_BYTES = (BN / 64) * 128 * 128;   // [BN/64][128 rows][128 B]
-    static constexpr int OFF_KV = Q_BYTES;
-    static constexpr int OFF_P = OFF_KV + NSTAGE * 2 * KV_TILE;
-    static constexpr int NBAR = 1 + 2 * NSTAGE + 2 + 2 + 1 + 1;
-    static constexpr int OFF_BAR = OFF_P + P_BYTES;
+    static constexpr int OFF_K = Q_BYTES;
+    static constexpr int OFF_V = OFF_K + NSTAGE * KV_TILE;
+    static constexpr int OFF_P = OFF_V + NSTAGE * KV_TILE;  // two P buffers
+    static constexpr int NBAR = 1 + 4 * NSTAGE + 2 + 2 + 2 + 2;
+    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int TMEM_COLS = 512;
     static constexpr int O_COL = 2 * BN;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 224;                // 4 softmax + K producer + MMA + V producer
     static_assert(O_COL + D <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(BN % 64 == 0 && D % 64 == 0, "tile shape");
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                             const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const TcArgs a) {
@@ -69,16 +74,19 @@ __global__ void __launch_bounds__(192, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t q_smem = sbase;
-    const uint32_t kv_smem = sbase + C::OFF_KV;
+    const uint32_t k_smem = sbase + C::OFF_K;
+    const uint32_t v_smem = sbase + C::OFF_V;
     const uint32_t p_smem = sbase + C::OFF_P;
-    const uint32_t bar0 = sbase + C::OFF_BAR;
-    const uint32_t bar_q = bar0;
-    const uint32_t bar_kv_full = bar0 + 8;
-    const uint32_t bar_kv_empty = bar_kv_full + 8 * C::NSTAGE;
-    const uint32_t bar_s_full = bar_kv_empty + 8 * C::NSTAGE;   // [2]
-    const uint32_t bar_s_free = bar_s_full + 16;                 // [2]
-    const uint32_t bar_p_full = bar_s_free + 16;
-    const uint32_t bar_o_done = bar_p_full + 8;
+    // barriers (each waited by one party in order, never two phases behind)
+    const uint32_t bar_q = sbase + C::OFF_BAR;
+    const uint32_t bar_k_full = bar_q + 8;                          // [NSTAGE]
+    const uint32_t bar_k_empty = bar_k_full + 8 * C::NSTAGE;        // [NSTAGE]
+    const uint32_t bar_v_full = bar_k_empty + 8 * C::NSTAGE;        // [NSTAGE]
+    const uint32_t bar_v_empty = bar_v_full + 8 * C::NSTAGE;        // [NSTAGE]
+    const uint32_t bar_s_full = bar_v_empty + 8 * C::NSTAGE;        // [2] S buffer
+    const uint32_t bar_s_free = bar_s_full + 16;                    // [2]
+    const uint32_t bar_p_full = bar_s_free + 16;                    // [2] P buffer
+    const uint32_t bar_o_done = bar_p_full + 16;                    // [2] PV of P buffer b done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
 
@@ -117,15 +125,17 @@ __global__ void __launch_bounds__(192, 1)
     if (tid == 0) {
         mbar_init(bar_q, 1);
         for (int s = 0; s < C::NSTAGE; ++s) {
-            mbar_init(bar_kv_full + 8 * s, 1);
-            mbar_init(bar_kv_empty + 8 * s, 1);
+            mbar_init(bar_k_full + 8 * s, 1);
+            mbar_init(bar_k_empty + 8 * s, 1);
+            mbar_init(bar_v_full + 8 * s, 1);
+            mbar_init(bar_v_empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_s_full + 8 * b, 1);
             mbar_init(bar_s_free + 8 * b, 4);
+            mbar_init(bar_p_full + 8 * b, 4);
+            mbar_init(bar_o_done + 8 * b, 1);
         }
-        mbar_init(bar_p_full, 4);
-        mbar_init(bar_o_done, 1);
         fence_barrier_init();
         *abort_flag = 0;
     }
@@ -133,26 +143,44 @@ __global__ void __launch_bounds__(192, 1)
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
+    if (C::M_USED < 128) {
+        // Q rows past the (query row, head) pairs are never loaded: make them
+        // zero so their score rows stay finite
+        constexpr int PAD = (128 - C::M_USED) * 8;   // 16-byte chunks per region
+        for (int c = 0; c < C::KCH; ++c)
+            for (int q = tid; q < PAD; q += C::THREADS)
+                *reinterpret_cast<uint4 *>(smem + c * 128 * 128 + C::M_USED * 128 + q * 16) =
+                    make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
-        // ============================================================ producer
+    if (warp == 4 || warp == 6) {
+        // ============================================================ producers
+        // warp 4 streams Q and the K tiles, warp 6 the V tiles; K stage j is
+        // released as soon as S(j) is done, V stage j after PV(j).
+        const bool is_k = (warp == 4);
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        const uint32_t bar_full = is_k ? bar_k_full : bar_v_full;
+        const uint32_t bar_empty = is_k ? bar_k_empty : bar_v_empty;
+        const uint32_t stage0 = is_k ? k_smem : v_smem;
         const int BR = a.box_rows;
         const int SUB = C::BN / BR;
-        const uint64_t pol_kv = policy_evict_last();   // K/V are re-read by other query blocks
+        const uint64_t pol_kv = policy_evict_last();   // re-read by the request's other blocks
         if (lane == 0) {
-            prefetch_tensormap(&qmap);
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
-            mbar_arrive_expect_tx(bar_q, C::KCH * C::M_USED * 128);
-            const uint64_t pol_q = policy_evict_first();
+            prefetch_tensormap(map);
+            if (is_k) {
+                prefetch_tensormap(&qmap);
+                mbar_arrive_expect_tx(bar_q, C::KCH * C::M_USED * 128);
+                const uint64_t pol_q = policy_evict_first();
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-                tma_load_3d(q_smem + c * 128 * 128, &qmap, c * 64, h * G, (int)row_base, bar_q,
-                            pol_q);
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_3d(q_smem + c * 128 * 128, &qmap, c * 64, h * G, (int)row_base,
+                                bar_q, pol_q);
+            }
         }
         const int32_t *bt = a.block_tables + (int64_t)r * a.max_blocks_per_seq;
         const int nsb_total = (kend + BR - 1) / BR;
@@ -166,15 +194,13 @@ __global__ void __launch_bounds__(192, 1)
             const int use = j / C::NSTAGE;
             int bad = 0;
             if (lane == 0 && use > 0)
-                bad = !mbar_wait(bar_kv_empty + 8 * st, (use - 1) & 1, a.err, abort_flag);
+                bad = !mbar_wait(bar_empty + 8 * st, (use - 1) & 1, a.err, abort_flag);
             if (__shfl_sync(0xffffffffu, bad, 0)) break;
             const int cnt = min(C::BN, kend - j * C::BN);
             const int nsub = (cnt + BR - 1) / BR;
-            if (lane == 0)
-                mbar_arrive_expect_tx(bar_kv_full + 8 * st, nsub * C::KCH * BR * 128 * 2);
+            if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * st, nsub * C::KCH * BR * 128);
             __syncwarp();
-            const uint32_t ks = kv_smem + st * 2 * C::KV_TILE;
-            const uint32_t vs = ks + C::KV_TILE;
+            const uint32_t dst = stage0 + st * C::KV_TILE;
             for (int u = 0; u < nsub; ++u) {
                 const int gsb = j * SUB + u;
                 if (gsb >= base + 32) {
@@ -186,20 +212,18 @@ __global__ void __launch_bounds__(192, 1)
                 if (lane == 0) {
                     const int row0 = page * bs + (gsb * BR) % bs;
 #pragma unroll
-                    for (int c = 0; c < C::KCH; ++c) {
-                        const uint32_t off = c * C::BN * 128 + u * BR * 128;
-                        tma_load_3d(ks + off, &kmap, c * 64, h, row0, bar_kv_full + 8 * st, pol_kv);
-                        tma_load_3d(vs + off, &vmap, c * 64, h, row0, bar_kv_full + 8 * st, pol_kv);
-                    }
+                    for (int c = 0; c < C::KCH; ++c)
+                        tma_load_3d(dst + c * C::BN * 128 + u * BR * 128, map, c * 64, h, row0,
+                                    bar_full + 8 * st, pol_kv);
                 }
             }
             __syncwarp();
             issued = j + 1;
         }
         if (lane == 0) {
-            mbar_drain(bar_q, 0, kWaitLimitCycles / 8);
+            if (is_k) mbar_drain(bar_q, 0, kWaitLimitCycles / 8);
             for (int j = max(0, issued - C::NSTAGE); j < issued; ++j)
-                mbar_drain(bar_kv_full + 8 * (j % C::NSTAGE), (j / C::NSTAGE) & 1,
+                mbar_drain(bar_full + 8 * (j % C::NSTAGE), (j / C::NSTAGE) & 1,
                            kWaitLimitCycles / 8);
         }
     } else if (warp == 5) {
@@ -209,27 +233,30 @@ __global__ void __launch_bounds__(192, 1)
             constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
             mbar_wait(bar_q, 0, a.err, abort_flag);
             auto issue_pv = [&](int jj) {
-                mbar_wait(bar_p_full, jj & 1, a.err, abort_flag);
-                tc_fence_after();
+                const int pb = jj & 1;
                 const int stp = jj % C::NSTAGE;
-                const uint32_t vs = kv_smem + stp * 2 * C::KV_TILE + C::KV_TILE;
+                mbar_wait(bar_p_full + 8 * pb, (jj >> 1) & 1, a.err, abort_flag);
+                mbar_wait(bar_v_full + 8 * stp, (jj / C::NSTAGE) & 1, a.err, abort_flag);
+                tc_fence_after();
+                const uint32_t vs = v_smem + stp * C::KV_TILE;
+                const uint32_t ps = p_smem + pb * C::P_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk) {
                     const uint64_t ad =
-                        smem_desc_sw128(p_smem + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
+                        smem_desc_sw128(ps + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(vs + kk * 16 * 128, C::BN * 128, 1024);
                     tc_mma_bf16(tmem + C::O_COL, ad, bd, IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(bar_o_done);
-                tc_commit(bar_kv_empty + 8 * stp);
+                tc_commit(bar_o_done + 8 * pb);
+                tc_commit(bar_v_empty + 8 * stp);
             };
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j % C::NSTAGE;
                 const int sb = j & 1;
-                mbar_wait(bar_kv_full + 8 * st, (j / C::NSTAGE) & 1, a.err, abort_flag);
+                mbar_wait(bar_k_full + 8 * st, (j / C::NSTAGE) & 1, a.err, abort_flag);
                 if (j >= 2) mbar_wait(bar_s_free + 8 * sb, ((j >> 1) - 1) & 1, a.err, abort_flag);
                 tc_fence_after();
-                const uint32_t ks = kv_smem + st * 2 * C::KV_TILE;
+                const uint32_t ks = k_smem + st * C::KV_TILE;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk & 3) * 32;   // 16 bf16 within the 128-B row
@@ -240,12 +267,14 @@ __global__ void __launch_bounds__(192, 1)
                     tc_mma_bf16(tmem + sb * C::BN, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bar_s_full + 8 * sb);
+                tc_commit(bar_k_empty + 8 * st);
                 if (j >= 1) issue_pv(j - 1);
             }
             issue_pv(ntiles - 1);
             // every MMA must be finished before TMEM is freed (bounded wait that
             // also holds on an aborted pipeline)
-            mbar_drain(bar_o_done, (ntiles - 1) & 1, kWaitLimitCycles / 8);
+            mbar_drain(bar_o_done + 8 * ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1,
+                       kWaitLimitCycles / 8);
         }
     } else {
         // ============================================================ softmax
@@ -254,10 +283,14 @@ __global__ void __launch_bounds__(192, 1)
         const bool row_ok = (m < C::M_USED) && (i < rows);
         const int qi = i0 + i;
         const int lim = min(N - 1, a.causal ? N - n + qi : N - 1);   // last visible key
+        // keys up to lim_all are visible to every row of the block
+        const int lim_all = min(N - 1, a.causal ? N - n + i0 : N - 1);
         const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const float qs = a.qscale;
         float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
         for (int j = 0; j < ntiles; ++j) {
             const int sb = j & 1;
+            const int pb = j & 1;
             const int st = j % C::NSTAGE;
             mbar_wait(bar_s_full + 8 * sb, (j >> 1) & 1, a.err, abort_flag);
             tc_fence_after();
@@ -269,14 +302,31 @@ __global__ void __launch_bounds__(192, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_s_free + 8 * sb);
 
+            // Tiles that reach past a row's last visible key are masked and scaled
+            // here (masked keys become -inf); fully visible tiles keep raw scores
+            // and are scaled inside the exponent.  sc = scale still to apply.
             const int kt0 = j * C::BN;
-            float tmax = -INFINITY;
+            const bool tmask = kt0 + C::BN - 1 > lim_all;
+            if (tmask) {
 #pragma unroll
-            for (int c = 0; c < C::BN; ++c) {
-                const bool vis = row_ok && (kt0 + c <= lim);
-                s[c] = vis ? s[c] * a.qscale : -INFINITY;
-                tmax = fmaxf(tmax, s[c]);
+                for (int c = 0; c < C::BN; ++c)
+                    s[c] = (row_ok && kt0 + c <= lim) ? s[c] * qs : -INFINITY;
             }
+            const float sc = tmask ? 1.f : qs;
+            // row max (8 independent chains) of sc * s, via max(s) or max(-s)
+            const bool neg = sc < 0.f;
+            float mx[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = neg ? -s[k] : s[k];
+#pragma unroll
+            for (int c = 8; c < C::BN; c += 8)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], neg ? -s[c + k] : s[c + k]);
+#pragma unroll
+            for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+                for (int q = 0; q < k; ++q) mx[q] = fmaxf(mx[q], mx[q + k]);
+            const float tmax = mx[0] == -INFINITY ? -INFINITY : mx[0] * fabsf(sc);
             const float m_new = fmaxf(m_run, tmax);
             m_run = m_new;
             const bool need = (m_new != -INFINITY) && (m_ref == -INFINITY || m_new > m_ref + 8.f);
@@ -285,20 +335,18 @@ __global__ void __launch_bounds__(192, 1)
             // before the PV MMA (a zero weight times NaN is still NaN).
             const int cnt = min(C::BN, kend - kt0);
             if (cnt < C::BN) {
-                mbar_wait(bar_kv_full + 8 * st, (j / C::NSTAGE) & 1, a.err, abort_flag);
-                uint8_t *vsp = smem + C::OFF_KV + st * 2 * C::KV_TILE + C::KV_TILE;
+                mbar_wait(bar_v_full + 8 * st, (j / C::NSTAGE) & 1, a.err, abort_flag);
+                uint8_t *vsp = smem + C::OFF_V + st * C::KV_TILE;
                 const int nchunk = (C::BN - cnt) * 8;     // 16-byte chunks per D-chunk region
                 for (int c = 0; c < C::KCH; ++c)
                     for (int q = tid; q < nchunk; q += 128)
                         *reinterpret_cast<uint4 *>(vsp + c * C::BN * 128 + cnt * 128 + q * 16) =
                             make_uint4(0, 0, 0, 0);
             }
-            // PV of the previous tile must be done before O or the P buffer change.
-            if (j >= 1) {
-                mbar_wait(bar_o_done, (j - 1) & 1, a.err, abort_flag);
-                tc_fence_after();
-            }
+            // O changes only when a row's reference max moves: then PV(j-1) must be done.
             if (j >= 1 && __any_sync(0xffffffffu, need)) {
+                mbar_wait(bar_o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, a.err, abort_flag);
+                tc_fence_after();
                 const float f = need ? (m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new)) : 1.f;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
@@ -315,29 +363,45 @@ __global__ void __launch_bounds__(192, 1)
                 l *= (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
                 m_ref = m_new;
             }
-            // P = 2^(s - m_ref) as bf16, row m of the K-major 128-byte-swizzled A tile
+            // P buffer pb was last read by PV(j-2)
+            if (j >= 2) mbar_wait(bar_o_done + 8 * pb, ((j >> 1) - 1) & 1, a.err, abort_flag);
+            // P = 2^(sc * s - m_ref) as bf16 (masked keys: 2^-inf = 0),
+            // row m of the K-major 128-byte-swizzled A tile
+            const float2 qs2 = make_float2(sc, sc);
+            const float mu = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            const float2 mu2 = make_float2(mu, mu);
+            float2 sum2[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sum2[k] = make_float2(0.f, 0.f);
+            const uint32_t ps = p_smem + pb * C::P_BYTES;
 #pragma unroll
             for (int k8 = 0; k8 < C::BN / 8; ++k8) {
-                float p[8];
+                uint32_t w4[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x = s[k8 * 8 + e];
-                    p[e] = (x == -INFINITY) ? 0.f : exp2f(x - m_ref);
-                    l += p[e];
+                for (int e = 0; e < 4; ++e) {
+                    float2 x = __ffma2_rn(make_float2(s[k8 * 8 + 2 * e], s[k8 * 8 + 2 * e + 1]),
+                                          qs2, mu2);
+                    x.x = ex2_approx(x.x);
+                    x.y = ex2_approx(x.y);
+                    sum2[e] = __fadd2_rn(sum2[e], x);
+                    w4[e] = pack_bf16x2(x.x, x.y);
                 }
-                const uint32_t addr = p_smem + (k8 >> 3) * 128 * 128 + m * 128 +
+                const uint32_t addr = ps + (k8 >> 3) * 128 * 128 + m * 128 +
                                       (((k8 & 7) ^ (m & 7)) << 4);
-                sts128(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                       pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+                sts128(addr, w4[0], w4[1], w4[2], w4[3]);
             }
+            const float2 sa = __fadd2_rn(sum2[0], sum2[1]);
+            const float2 sbb = __fadd2_rn(sum2[2], sum2[3]);
+            l += (sa.x + sa.y) + (sbb.x + sbb.y);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_p_full);
+            if (lane == 0) mbar_arrive(bar_p_full + 8 * pb);
         }
         // ---- epilogue: out = O / (l + sink term)
         if (ntiles > 0) {
-            mbar_wait(bar_o_done, (ntiles - 1) & 1, a.err, abort_flag);
+            mbar_wait(bar_o_done + 8 * ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, a.err,
+                      abort_flag);
             tc_fence_after();
         }
         float scale_out = 0.f;

@@ -248,3 +248,14 @@ def test_workload_mixed_step_full_size():
 def test_workload_long_decode_sinks_full_size(P):
     """4 x 65536 + 12 x ~4600 contexts, (24, 4, 256), bs 32, sinks; P in {256, 512, none}."""
     check_step(wl.workload(4, partition_size=P))
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.07])
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+def test_zero_and_negative_scale(scale, dtype):
+    """scale 0 gives plain prefix means; a negative scale flips the ordering of
+    the scores.  Both must hold on the decode and the multi-query kernels."""
+    w = wl.random_small(86, dtype=dtype, num_seqs=5, head_dim=128, num_q_heads=8,
+                        num_kv_heads=2, max_prior=400, max_q=6, with_sinks=True)
+    w.scale = scale
+    check_step(w)
