@@ -344,6 +344,7 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
         CUtensorMap qmap, kmap_tc, vmap_tc;
         st = make_query_map(&qmap, q, head_dim, num_q_heads, total_q, group, bq);
         if (st != PA_OK) return st;
+        // one box per (page, 128-byte chunk)
         st = make_cache_map(&kmap_tc, key_cache, dtype, head_dim, num_kv_heads,
                             num_blocks * block_size, tc_box);
         if (st != PA_OK) return st;
@@ -365,13 +366,25 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
         ta.causal = causal ? 1 : 0;
         ta.box_rows = tc_box;
         ta.err = dev.err;
-        // virtual query blocks: request r owns blocks cu_seqlens_q[r] / bq + r ...
-        const dim3 grid((unsigned)(total_q / bq + num_seqs), num_kv_heads, 1);
-        switch (head_dim) {
-            case 64: ce = launch_prefill_tc_d64(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
-            case 128: ce = launch_prefill_tc_d128(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
-            default: ce = launch_prefill_tc_d256(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
+        auto launch_tc = [&](bool paired, dim3 grid) -> cudaError_t {
+            switch (head_dim) {
+                case 64: return launch_prefill_tc_d64(group, paired, qmap, kmap_tc, vmap_tc, ta,
+                                                      grid, s);
+                case 128: return launch_prefill_tc_d128(group, paired, qmap, kmap_tc, vmap_tc, ta,
+                                                        grid, s);
+                default: return launch_prefill_tc_d256(group, paired, qmap, kmap_tc, vmap_tc, ta,
+                                                       grid, s);
+            }
+        };
+        // requests whose rows span two or more query blocks: CTA pairs sharing
+        // every K/V tile; virtual pairs: request r owns cu_seqlens_q[r] / (2 bq) + r ...
+        if (max_seqlen_q > bq) {
+            ce = launch_tc(true, dim3((unsigned)(2 * (total_q / (2 * bq) + num_seqs)),
+                                      num_kv_heads, 1));
+            if (ce != cudaSuccess) return cuda_fail(ce, "paged_prefill_tc (paired) launch");
         }
+        // requests whose rows fit one query block (verify windows, short chunks)
+        ce = launch_tc(false, dim3((unsigned)num_seqs, num_kv_heads, 1));
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_prefill_tc launch");
     } else if (max_seqlen_q > 1) {
         a.mode = 1;

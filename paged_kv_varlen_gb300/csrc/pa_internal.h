@@ -103,9 +103,12 @@ __host__ __device__ constexpr int gcd_int(int a, int b) { return b == 0 ? a : gc
 // Message returned by pa_last_error_string() on this thread.
 void set_last_error(const char *msg);
 
-// Tensor-core kernel for multi-query rows, per head_dim (bf16 only).
+// Tensor-core kernel for multi-query rows, per head_dim (bf16 only).  paired:
+// clusters of two CTAs over requests with two or more query blocks (grid.x =
+// 2 * (total_q / (2 * BQ) + num_seqs)); single: one CTA per request whose rows
+// fit one block (grid.x = num_seqs).  grid.y = num_kv_heads.
 #define PA_DECLARE_TC(NAME) \
-    cudaError_t NAME(int group, const CUtensorMap &qmap, const CUtensorMap &kmap, \
+    cudaError_t NAME(int group, bool paired, const CUtensorMap &qmap, const CUtensorMap &kmap, \
                      const CUtensorMap &vmap, const TcArgs &a, dim3 grid, cudaStream_t stream);
 PA_DECLARE_TC(launch_prefill_tc_d64)
 PA_DECLARE_TC(launch_prefill_tc_d128)

@@ -45,7 +45,9 @@ struct TcCfg {
     static constexpr int BN = tc_tile_keys(D);         // keys per K/V tile
     static constexpr int KCH = D / 64;                 // 128-byte chunks of a head row
     static constexpr int Q_BYTES = KCH * 128 * 128;    // [KCH][128 rows][128 B]
-    static constexpr int KV_TILE = KCH * BN * 128;     // [KCH][BN rows][128 B]
+    // K/V tile layout [KCH][BN rows][128 B] (the tensor cores' 128-byte-swizzled
+    // canonical layout), one TMA box per (page, 128-byte chunk).
+    static constexpr int KV_TILE = KCH * BN * 128;
     static constexpr int NSTAGE = D >= 128 ? 2 : 3;    // K stages (and as many V stages)
     static constexpr int P_BYTES = (BN / 64) * 128 * 128;   // [BN/64][128 rows][128 B]
     static constexpr int OFF_K = Q_BYTES;
@@ -63,7 +65,11 @@ struct TcCfg {
     static_assert(BN % 64 == 0 && D % 64 == 0, "tile shape");
 };
 
-template <int D, int G>
+// PAIR: a cluster of two CTAs takes two adjacent query blocks of one request
+// and KV head; both walk the same K/V tiles and each CTA loads half of every
+// tile with TMA multicast into both, halving the per-SM K/V traffic.  Without
+// PAIR a CTA takes a request whose rows fit one query block.
+template <int D, int G, bool PAIR>
 __global__ void __launch_bounds__(224, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                             const __grid_constant__ CUtensorMap kmap,
@@ -98,37 +104,71 @@ __global__ void __launch_bounds__(224, 1)
     const int bs = a.block_size;
 
     // ---------------------------------------------------------------- work item
-    // Virtual block t belongs to the last request r with cu[r] / BQ + r <= t.
-    const int t = blockIdx.x;
-    int lo = 0, hi = a.num_seqs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.cu_seqlens_q[mid] / C::BQ + mid <= t) lo = mid;
-        else hi = mid - 1;
+    int r, i0, rows, kend, rot_seed;
+    if (PAIR) {
+        // Virtual pair p belongs to the last request r with cu[r] / (2 BQ) + r <= p;
+        // the two CTAs of a cluster (rank 0, 1) take blocks 2l and 2l + 1.
+        const int p = blockIdx.x >> 1;
+        const int rank = blockIdx.x & 1;
+        int lo = 0, hi = a.num_seqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.cu_seqlens_q[mid] / (2 * C::BQ) + mid <= p) lo = mid;
+            else hi = mid - 1;
+        }
+        r = lo;
+        const int c0r = a.cu_seqlens_q[r];
+        const int nr = a.cu_seqlens_q[r + 1] - c0r;
+        const int nblk = (nr + C::BQ - 1) / C::BQ;
+        const int npairs = (nblk + 1) / 2;
+        const int lp = p - (c0r / (2 * C::BQ) + r);
+        if (nblk < 2 || lp < 0 || lp >= npairs) return;   // whole cluster leaves together
+        const int lpp = npairs - 1 - lp;                    // heaviest pair first
+        const int qb = 2 * lpp + rank;                      // may be past the last block
+        const int qb_hi = min(2 * lpp + 1, nblk - 1);       // the pair's heavier block
+        i0 = qb * C::BQ;
+        rows = qb < nblk ? min(C::BQ, nr - i0) : 0;
+        int Nr = a.seq_lens_k[r];
+        Nr = max(0, min(Nr, a.max_blocks_per_seq * bs));
+        const int i0_hi = qb_hi * C::BQ;
+        const int rows_hi = min(C::BQ, nr - i0_hi);
+        kend = max(0, a.causal ? min(Nr, Nr - nr + i0_hi + rows_hi) : Nr);
+        rot_seed = p;
+    } else {
+        r = blockIdx.x;
+        const int nr = a.cu_seqlens_q[r + 1] - a.cu_seqlens_q[r];
+        if (nr <= 1 || nr > C::BQ) return;                 // decode rows / paired launch
+        int Nr = a.seq_lens_k[r];
+        Nr = max(0, min(Nr, a.max_blocks_per_seq * bs));
+        i0 = 0;
+        rows = nr;
+        kend = max(0, a.causal ? min(Nr, Nr - nr + rows) : Nr);
+        rot_seed = blockIdx.x;
     }
-    const int r = lo;
     const int c0 = a.cu_seqlens_q[r];
     const int n = a.cu_seqlens_q[r + 1] - c0;
-    const int nblk = (n + C::BQ - 1) / C::BQ;
-    const int local = t - (c0 / C::BQ + r);
-    if (n <= 1 || local < 0 || local >= nblk) return;    // single-query rows: decode kernel
-    const int qb = nblk - 1 - local;                      // heaviest block first
-    const int i0 = qb * C::BQ;
-    const int rows = min(C::BQ, n - i0);
     int N = a.seq_lens_k[r];
     N = max(0, min(N, a.max_blocks_per_seq * bs));
-    const int kend = max(0, a.causal ? min(N, N - n + i0 + rows) : N);
     const int ntiles = (kend + C::BN - 1) / C::BN;
     const int64_t row_base = (int64_t)c0 + i0;
+    // The blocks of one request read the same keys: each starts at its own tile
+    // and wraps around, so they do not all hit the same L2 lines at once (the
+    // online softmax does not depend on the order of the tiles).  Both CTAs of a
+    // pair use the same order.
+    const int rot = ntiles > 1
+        ? (int)(((uint32_t)rot_seed * 2654435761u + (uint32_t)blockIdx.y * 40503u) % ntiles)
+        : 0;
+    auto tile_of = [&](int j) { const int jt = j + rot; return jt >= ntiles ? jt - ntiles : jt; };
+    constexpr uint16_t kPairMask = 0x3;
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
         mbar_init(bar_q, 1);
         for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(bar_k_full + 8 * s, 1);
-            mbar_init(bar_k_empty + 8 * s, 1);
+            mbar_init(bar_k_empty + 8 * s, PAIR ? 2 : 1);   // both CTAs release a stage
             mbar_init(bar_v_full + 8 * s, 1);
-            mbar_init(bar_v_empty + 8 * s, 1);
+            mbar_init(bar_v_empty + 8 * s, PAIR ? 2 : 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_s_full + 8 * b, 1);
@@ -155,6 +195,7 @@ __global__ void __launch_bounds__(224, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -168,7 +209,6 @@ __global__ void __launch_bounds__(224, 1)
         const uint32_t bar_empty = is_k ? bar_k_empty : bar_v_empty;
         const uint32_t stage0 = is_k ? k_smem : v_smem;
         const int BR = a.box_rows;
-        const int SUB = C::BN / BR;
         const uint64_t pol_kv = policy_evict_last();   // re-read by the request's other blocks
         if (lane == 0) {
             prefetch_tensormap(map);
@@ -183,41 +223,50 @@ __global__ void __launch_bounds__(224, 1)
             }
         }
         const int32_t *bt = a.block_tables + (int64_t)r * a.max_blocks_per_seq;
-        const int nsb_total = (kend + BR - 1) / BR;
-        auto page_of = [&](int gsb) -> int { return gsb < nsb_total ? bt[(gsb * BR) / bs] : 0; };
-        int base = 0;
-        int cur = page_of(lane);
-        int nxt = page_of(32 + lane);
+        // page ids of a tile's boxes: lane u holds box u's page, loaded one tile ahead
+        auto pages_of = [&](int j) -> int {
+            if (j >= ntiles) return 0;
+            const int kt = tile_of(j) * C::BN;
+            const int nsub = (min(C::BN, kend - kt) + BR - 1) / BR;
+            return lane < nsub ? bt[(kt + lane * BR) / bs] : 0;
+        };
+        int pg_cur = pages_of(0);
         int issued = 0;
         for (int j = 0; j < ntiles; ++j) {
+            const int pg_next = pages_of(j + 1);
             const int st = j % C::NSTAGE;
             const int use = j / C::NSTAGE;
             int bad = 0;
             if (lane == 0 && use > 0)
                 bad = !mbar_wait(bar_empty + 8 * st, (use - 1) & 1, a.err, abort_flag);
             if (__shfl_sync(0xffffffffu, bad, 0)) break;
-            const int cnt = min(C::BN, kend - j * C::BN);
+            const int kt = tile_of(j) * C::BN;
+            const int cnt = min(C::BN, kend - kt);
             const int nsub = (cnt + BR - 1) / BR;
             if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * st, nsub * C::KCH * BR * 128);
             __syncwarp();
             const uint32_t dst = stage0 + st * C::KV_TILE;
+            // paired: rank 0 loads the first half of the boxes, rank 1 the rest,
+            // each multicast to both CTAs (every CTA expects the whole tile)
+            const int u_lo = PAIR ? ((blockIdx.x & 1) ? (nsub + 1) / 2 : 0) : 0;
+            const int u_hi = PAIR ? ((blockIdx.x & 1) ? nsub : (nsub + 1) / 2) : nsub;
             for (int u = 0; u < nsub; ++u) {
-                const int gsb = j * SUB + u;
-                if (gsb >= base + 32) {
-                    base += 32;
-                    cur = nxt;
-                    nxt = page_of(base + 32 + lane);
-                }
-                const int page = __shfl_sync(0xffffffffu, cur, gsb - base);
-                if (lane == 0) {
-                    const int row0 = page * bs + (gsb * BR) % bs;
+                const int page = __shfl_sync(0xffffffffu, pg_cur, u);
+                if (lane == 0 && u >= u_lo && u < u_hi) {
+                    const int row0 = page * bs + (kt + u * BR) % bs;
 #pragma unroll
-                    for (int c = 0; c < C::KCH; ++c)
-                        tma_load_3d(dst + c * C::BN * 128 + u * BR * 128, map, c * 64, h, row0,
-                                    bar_full + 8 * st, pol_kv);
+                    for (int c = 0; c < C::KCH; ++c) {
+                        const uint32_t d = dst + c * C::BN * 128 + u * BR * 128;
+                        if (PAIR)
+                            tma_load_3d_mc(d, map, c * 64, h, row0, bar_full + 8 * st,
+                                           kPairMask, pol_kv);
+                        else
+                            tma_load_3d(d, map, c * 64, h, row0, bar_full + 8 * st, pol_kv);
+                    }
                 }
             }
             __syncwarp();
+            pg_cur = pg_next;
             issued = j + 1;
         }
         if (lane == 0) {
@@ -244,11 +293,14 @@ __global__ void __launch_bounds__(224, 1)
                 for (int kk = 0; kk < C::BN / 16; ++kk) {
                     const uint64_t ad =
                         smem_desc_sw128(ps + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
+                    // V as MN-major B: atoms of 64 d x 8 keys; LBO steps d-chunks, SBO
+                    // steps 8-key groups; one k-step is 16 keys
                     const uint64_t bd = smem_desc_sw128(vs + kk * 16 * 128, C::BN * 128, 1024);
                     tc_mma_bf16(tmem + C::O_COL, ad, bd, IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar_o_done + 8 * pb);
-                tc_commit(bar_v_empty + 8 * stp);
+                if (PAIR) tc_commit_mc(bar_v_empty + 8 * stp, kPairMask);
+                else tc_commit(bar_v_empty + 8 * stp);
             };
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j % C::NSTAGE;
@@ -267,7 +319,8 @@ __global__ void __launch_bounds__(224, 1)
                     tc_mma_bf16(tmem + sb * C::BN, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bar_s_full + 8 * sb);
-                tc_commit(bar_k_empty + 8 * st);
+                if (PAIR) tc_commit_mc(bar_k_empty + 8 * st, kPairMask);
+                else tc_commit(bar_k_empty + 8 * st);
                 if (j >= 1) issue_pv(j - 1);
             }
             issue_pv(ntiles - 1);
@@ -305,7 +358,7 @@ __global__ void __launch_bounds__(224, 1)
             // Tiles that reach past a row's last visible key are masked and scaled
             // here (masked keys become -inf); fully visible tiles keep raw scores
             // and are scaled inside the exponent.  sc = scale still to apply.
-            const int kt0 = j * C::BN;
+            const int kt0 = tile_of(j) * C::BN;
             const bool tmask = kt0 + C::BN - 1 > lim_all;
             if (tmask) {
 #pragma unroll
@@ -337,11 +390,13 @@ __global__ void __launch_bounds__(224, 1)
             if (cnt < C::BN) {
                 mbar_wait(bar_v_full + 8 * st, (j / C::NSTAGE) & 1, a.err, abort_flag);
                 uint8_t *vsp = smem + C::OFF_V + st * C::KV_TILE;
-                const int nchunk = (C::BN - cnt) * 8;     // 16-byte chunks per D-chunk region
-                for (int c = 0; c < C::KCH; ++c)
-                    for (int q = tid; q < nchunk; q += 128)
-                        *reinterpret_cast<uint4 *>(vsp + c * C::BN * 128 + cnt * 128 + q * 16) =
-                            make_uint4(0, 0, 0, 0);
+                const int nchunk = (C::BN - cnt) * C::KCH * 8;   // 16-byte pieces to clear
+                for (int q = tid; q < nchunk; q += 128) {
+                    const int k = cnt + q / (C::KCH * 8);          // key row of the tile
+                    const int c = (q >> 3) % C::KCH;               // 128-byte chunk of the row
+                    const int off = c * C::BN * 128 + k * 128;
+                    *reinterpret_cast<uint4 *>(vsp + off + (q & 7) * 16) = make_uint4(0, 0, 0, 0);
+                }
             }
             // O changes only when a row's reference max moves: then PV(j-1) must be done.
             if (j >= 1 && __any_sync(0xffffffffu, need)) {
@@ -446,38 +501,60 @@ __global__ void __launch_bounds__(224, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
+    // no CTA of a pair leaves while its peer may still multicast into it or
+    // arrive on its barriers
+    if (PAIR) cluster_sync();
 }
 
-template <int D, int G>
+template <int D, int G, bool PAIR>
 cudaError_t launch_prefill_tc_t(const CUtensorMap &qmap, const CUtensorMap &kmap,
                                 const CUtensorMap &vmap, const TcArgs &a, dim3 grid,
                                 cudaStream_t stream) {
     using C = TcCfg<D, G>;
-    auto kern = paged_prefill_tc_kernel<D, G>;
+    auto kern = paged_prefill_tc_kernel<D, G, PAIR>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        if (PAIR) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+            if (e != cudaSuccess) return e;
+        }
         configured = true;
     }
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qmap, kmap, vmap, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool PAIR>
 cudaError_t launch_prefill_tc_group(int group, const CUtensorMap &qmap, const CUtensorMap &kmap,
                                     const CUtensorMap &vmap, const TcArgs &a, dim3 grid,
                                     cudaStream_t stream) {
     switch (group) {
-        case 1: return launch_prefill_tc_t<D, 1>(qmap, kmap, vmap, a, grid, stream);
-        case 2: return launch_prefill_tc_t<D, 2>(qmap, kmap, vmap, a, grid, stream);
-        case 3: return launch_prefill_tc_t<D, 3>(qmap, kmap, vmap, a, grid, stream);
-        case 4: return launch_prefill_tc_t<D, 4>(qmap, kmap, vmap, a, grid, stream);
-        case 5: return launch_prefill_tc_t<D, 5>(qmap, kmap, vmap, a, grid, stream);
-        case 6: return launch_prefill_tc_t<D, 6>(qmap, kmap, vmap, a, grid, stream);
-        case 7: return launch_prefill_tc_t<D, 7>(qmap, kmap, vmap, a, grid, stream);
-        case 8: return launch_prefill_tc_t<D, 8>(qmap, kmap, vmap, a, grid, stream);
+        case 1: return launch_prefill_tc_t<D, 1, PAIR>(qmap, kmap, vmap, a, grid, stream);
+        case 2: return launch_prefill_tc_t<D, 2, PAIR>(qmap, kmap, vmap, a, grid, stream);
+        case 3: return launch_prefill_tc_t<D, 3, PAIR>(qmap, kmap, vmap, a, grid, stream);
+        case 4: return launch_prefill_tc_t<D, 4, PAIR>(qmap, kmap, vmap, a, grid, stream);
+        case 5: return launch_prefill_tc_t<D, 5, PAIR>(qmap, kmap, vmap, a, grid, stream);
+        case 6: return launch_prefill_tc_t<D, 6, PAIR>(qmap, kmap, vmap, a, grid, stream);
+        case 7: return launch_prefill_tc_t<D, 7, PAIR>(qmap, kmap, vmap, a, grid, stream);
+        case 8: return launch_prefill_tc_t<D, 8, PAIR>(qmap, kmap, vmap, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
