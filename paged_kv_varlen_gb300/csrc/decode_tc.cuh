@@ -1,0 +1,810 @@
+// decode_tc.cuh -- single-query (decode) requests on the 5th-generation
+// tensor cores, bf16.
+//
+// What it computes (kwkr.cn, "What is Paged Attention": the GQA decode section
+// and trick 4; aisignalhub.me, "packed queries and paged KV"): for every
+// decode request r and query head, softmax(scale * q K^T) V over the request's
+// paged keys -- or, with the keys cut into partitions of P, one partial per
+// partition (log2-domain reference max, exp-sum, normalised output) for the
+// shared split-KV reduce.
+//
+// GB300 design (persistent: one CTA per SM, 288 threads)
+//  * A work item is (request, KV head, partition).  Every CTA scans the batch
+//    once, weighs each item by its key tiles plus one, and takes, in order,
+//    the items whose cumulative work starts inside its 1/gridDim share.
+//  * Keys are the MMA rows: S^T[128 keys x 16] = K_tile . Q^T with the G query
+//    heads of the KV head padded to N = 16, so one M = 128 MMA per 16-dim step
+//    serves the whole GQA group however small G is; O^T[d x 16] += V^T . P^T
+//    reads the V tile in place as an MN-major A operand.  The CUDA cores only
+//    see G scores per key instead of G * D multiply-adds.
+//  * Warps 4-7 (producers) gather the K and V tiles of all the CTA's items
+//    into one ring of 32 KB stages (128 keys x 128 dims, the tensor cores'
+//    128-byte-swizzled layout) with 16-byte cp.async copies: a 16-token page
+//    holds only 2 KB of one head's K, and TMA boxes that small are issued too
+//    slowly to reach the HBM rate from one SM.  The four warps fill every
+//    stage together, in sequence order, each a quarter of its keys; a warp
+//    signals a stage (wait_group + proxy fence, then one arrival) once it has
+//    issued LAG more, and never blocks while it holds an un-signalled stage.
+//    The page ids of the next tile and the next request's lengths are loaded
+//    a tile / a request ahead.  Rows past a tile's last key are zero-filled
+//    for V (a zero weight times a NaN pool slot would still be NaN) and left
+//    alone for K (masked).  Q comes once per item by TMA.
+//  * Warp 8 (MMA) allocates TMEM, issues S^T into one of two TMEM buffers and
+//    O^T into the accumulator of the item's parity; commits release stages.
+//  * Warps 0-3 (one thread per key = TMEM lane): scale S^T into the log2
+//    domain, take each head's tile max across the four warps, keep a
+//    reference max that moves only when the max grows by more than 2^8
+//    (then O^T and the running sums are rescaled), write P^T as bf16, and at
+//    the end of an item sum the exp-sums and write the output or the partial.
+//  * Every barrier wait is bounded (pa::mbar_wait); nothing spins forever.
+#pragma once
+
+#include <climits>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+#include "tc_common.cuh"
+
+namespace pa {
+
+template <int D>
+struct DtcCfg {
+    static constexpr int KS = D / 128;             // 128-dim chunks of a K (or V) row
+    static constexpr int KCH = D / 64;             // 64-dim (128-byte) sub-chunks
+    static constexpr int BN = 128;                 // keys per tile = MMA M
+    static constexpr int NP = 16;                  // MMA N: query heads padded to 16
+    static constexpr int SLOT = BN * 256;          // ring stage: 128 keys x 128 dims bf16
+    static constexpr int SUB = BN * 128;           // one 64-dim sub-chunk of a stage
+    static constexpr int NSLOT = 6;
+    static constexpr int Q_BUF = KCH * NP * 128;   // [KCH][16 rows][128 B]
+    static constexpr int P_BUF = 2 * NP * 128;     // [2 key halves][16 rows][128 B]
+    static constexpr int OFF_Q = NSLOT * SLOT;     // two Q^T buffers
+    static constexpr int OFF_P = OFF_Q + 2 * Q_BUF;   // two P^T buffers
+    static constexpr int OFF_BAR = OFF_P + 2 * P_BUF;
+    static constexpr int NBAR = 2 * NSLOT + 7 * 2;
+    static constexpr int OFF_RED = OFF_BAR + NBAR * 8;   // float [2][4][8] max, [2][4][8] sum
+    static constexpr int OFF_MISC = OFF_RED + 2 * 2 * 4 * 8 * 4;
+    static constexpr int SMEM_BYTES = OFF_MISC + 128 + 1024;   // + alignment slack
+    static constexpr int THREADS = 288;            // 4 softmax + 4 producer + 1 MMA warps
+    static constexpr int LAG = 2;                  // stages a producer warp signals late
+    static constexpr int S_COL = 0;                // two S^T buffers of NP columns
+    static constexpr int O_COL = 2 * NP;           // two O^T accumulators of KS * NP columns
+    static constexpr int TMEM_COLS = 128;
+    static_assert(O_COL + 2 * KS * NP <= TMEM_COLS, "TMEM columns");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && Q_BUF % 1024 == 0, "swizzle atoms");
+};
+
+// Work of one decode request: its (partition, KV head) items, ordered
+// partition-major, each weighed by its tiles plus one.
+struct DtcReq {
+    int items;   // 0 when the request has no decode work here
+    int np;      // partitions
+    int N;       // keys
+    int wfull;   // work of an item of a full partition
+    int wlast;   // work of an item of the last partition
+};
+
+// c0, c1 = cu_seqlens_q[r], cu_seqlens_q[r + 1]; sl = seq_lens_k[r]
+__device__ __forceinline__ DtcReq dtc_request_from(const DecodeTcArgs &a, int c0, int c1, int sl) {
+    DtcReq q = {0, 0, 0, 0, 0};
+    if (c1 - c0 != 1) return q;                       // multi-query request: other kernel
+    int N = max(0, min(sl, a.max_blocks_per_seq * a.block_size));
+    q.N = N;
+    const int P = a.partition_size;
+    if (P > 0) {
+        // partials exist for max_parts partitions only (the reduce reads no more)
+        N = min(N, a.max_parts * P);
+        q.N = N;
+        q.np = (N + P - 1) / P;
+        if (q.np == 0) return q;                      // no keys: the reduce writes zeros
+        q.wfull = (P + 127) / 128 + 1;
+        q.wlast = (N - (q.np - 1) * P + 127) / 128 + 1;
+    } else {
+        q.np = 1;                                     // one item, even with no keys
+        q.wfull = q.wlast = (N + 127) / 128 + 1;
+    }
+    q.items = q.np * a.num_kv_heads;
+    return q;
+}
+
+__device__ __forceinline__ DtcReq dtc_request(const DecodeTcArgs &a, int r) {
+    return dtc_request_from(a, a.cu_seqlens_q[r], a.cu_seqlens_q[r + 1], a.seq_lens_k[r]);
+}
+
+__device__ __forceinline__ int64_t dtc_work(const DtcReq &q, int hkv) {
+    return q.items == 0 ? 0 : ((int64_t)(q.np - 1) * q.wfull + q.wlast) * hkv;
+}
+
+// First item of q whose start (relative to the request) is >= off; *start is
+// that start.  Returns q.items when there is none.
+__device__ __forceinline__ int dtc_first_from(const DtcReq &q, int hkv, int64_t off,
+                                              int64_t *start) {
+    const int64_t nf = (int64_t)(q.np - 1) * hkv;   // items of full partitions
+    const int64_t wf = nf * q.wfull;
+    int64_t k;
+    if (off <= 0) k = 0;
+    else if (off <= wf) k = (off + q.wfull - 1) / q.wfull;
+    else k = nf + (off - wf + q.wlast - 1) / q.wlast;
+    *start = k <= nf ? k * q.wfull : wf + (k - nf) * q.wlast;
+    return (int)(k < q.items ? k : q.items);
+}
+
+// A position in the CTA's sequence of items.  The next request's lengths are
+// loaded when a request is entered, so moving on never waits for memory.
+struct DtcIter {
+    int r, k;          // request, item index inside the request
+    int64_t s;         // cumulative work before the item
+    DtcReq q;
+    int h, p, k0, k1, ntiles;
+    int64_t row;       // the request's packed query row (cu_seqlens_q[r])
+    int cu1;           // cu_seqlens_q[r + 1]
+    int pf_cu, pf_sl;  // cu_seqlens_q[r + 2], seq_lens_k[r + 1] (in flight)
+};
+
+__device__ __forceinline__ void dtc_enter(const DecodeTcArgs &a, DtcIter &it, int r, int c0,
+                                          int c1, int sl) {
+    it.r = r;
+    it.row = c0;
+    it.cu1 = c1;
+    it.q = dtc_request_from(a, c0, c1, sl);
+    if (r + 1 < a.num_seqs) {
+        it.pf_cu = __ldg(a.cu_seqlens_q + r + 2);
+        it.pf_sl = __ldg(a.seq_lens_k + r + 1);
+    }
+}
+
+__device__ __forceinline__ void dtc_fill(const DecodeTcArgs &a, DtcIter &it) {
+    it.p = it.k / a.num_kv_heads;
+    it.h = it.k - it.p * a.num_kv_heads;
+    if (a.partition_size > 0) {
+        it.k0 = it.p * a.partition_size;
+        it.k1 = min(it.q.N, it.k0 + a.partition_size);
+    } else {
+        it.k0 = 0;
+        it.k1 = it.q.N;
+    }
+    it.ntiles = (it.k1 - it.k0 + 127) / 128;
+}
+
+__device__ __forceinline__ void dtc_next(const DecodeTcArgs &a, DtcIter &it) {
+    it.s += (it.k < (it.q.np - 1) * a.num_kv_heads) ? it.q.wfull : it.q.wlast;
+    if (++it.k >= it.q.items) {
+        it.k = 0;
+        do {
+            const int r = it.r + 1;
+            if (r >= a.num_seqs) {
+                it.r = r;
+                return;
+            }
+            dtc_enter(a, it, r, it.cu1, it.pf_cu, it.pf_sl);
+        } while (it.q.items == 0);
+    }
+    dtc_fill(a, it);
+}
+
+// Inclusive scan over the block's threads; *total = the block's sum.
+template <int NT>
+__device__ __forceinline__ int64_t dtc_block_scan(int64_t v, long long *scratch, int64_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    long long before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const long long t = scratch[w];
+        if (w < warp) before += t;
+        tot += t;
+    }
+    __syncthreads();   // scratch is reused by the next scan
+    *total = tot;
+    return x + before;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(288, 1)
+    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap, const DecodeTcArgs a) {
+    using C = DtcCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t ring = sbase;
+    const uint32_t q_smem = sbase + C::OFF_Q;
+    const uint32_t p_smem = sbase + C::OFF_P;
+    // barriers (each waited by its parties in order, never two phases behind)
+    const uint32_t bar_full = sbase + C::OFF_BAR;              // [NSLOT] stage loaded
+    const uint32_t bar_empty = bar_full + 8 * C::NSLOT;        // [NSLOT] stage read
+    const uint32_t bar_q_full = bar_empty + 8 * C::NSLOT;      // [2] Q^T loaded
+    const uint32_t bar_q_empty = bar_q_full + 16;              // [2] last S^T of the item done
+    const uint32_t bar_s_full = bar_q_empty + 16;              // [2] S^T in TMEM
+    const uint32_t bar_s_free = bar_s_full + 16;               // [2] S^T read
+    const uint32_t bar_p_full = bar_s_free + 16;               // [2] P^T written
+    const uint32_t bar_o_done = bar_p_full + 16;               // [2] PV that read P buffer b done
+    const uint32_t bar_o_full = bar_o_done + 16;               // [2] item's last PV done
+    float *red_max = reinterpret_cast<float *>(smem + C::OFF_RED);   // [2][4 warps][8]
+    float *red_sum = red_max + 64;                                   // [2][4 warps][8]
+    uint8_t *misc = smem + C::OFF_MISC;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 8);
+    int *found = reinterpret_cast<int *>(misc + 16);
+    int *plan_rk = reinterpret_cast<int *>(misc + 24);               // first item: r, k
+    long long *plan_s = reinterpret_cast<long long *>(misc + 32);    // its start; range end
+    long long *scratch = reinterpret_cast<long long *>(misc + 48);   // [9]
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int S = a.num_seqs;
+    const int hkv = a.num_kv_heads;
+
+    // ---------------------------------------------------------------- setup
+    if (tid == 0) {
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(bar_full + 8 * s, 4);    // one arrival per producer warp
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_q_full + 8 * b, 1);
+            mbar_init(bar_q_empty + 8 * b, 1);
+            mbar_init(bar_s_full + 8 * b, 1);
+            mbar_init(bar_s_free + 8 * b, 4);
+            mbar_init(bar_p_full + 8 * b, 4);
+            mbar_init(bar_o_done + 8 * b, 1);
+            mbar_init(bar_o_full + 8 * b, 1);
+        }
+        fence_barrier_init();
+        *abort_flag = 0;
+        *found = INT_MAX;
+        plan_rk[0] = S;   // no item unless one is found below
+        plan_rk[1] = 0;
+        plan_s[0] = 0;
+        plan_s[1] = 0;
+    }
+    if (warp == 8) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    // Q^T and P^T rows past the G heads are never written: make them zero once
+    // so the padded MMA columns stay finite.
+    for (int i = tid; i < (2 * C::Q_BUF + 2 * C::P_BUF) / 16; i += C::THREADS)
+        *reinterpret_cast<uint4 *>(smem + C::OFF_Q + 16 * i) = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+
+    // ---- this CTA's items: those whose cumulative work starts in [lo, hi)
+    {
+        int64_t acc = 0;
+        for (int r = tid; r < S; r += C::THREADS) acc += dtc_work(dtc_request(a, r), hkv);
+        int64_t W;
+        dtc_block_scan<C::THREADS>(acc, scratch, &W);   // (also orders the setup writes)
+        const int64_t nb = gridDim.x, b = blockIdx.x;
+        const int64_t lo = (W / nb) * b + (W % nb) * b / nb;
+        const int64_t hi = (W / nb) * (b + 1) + (W % nb) * (b + 1) / nb;
+        if (tid == 0) plan_s[1] = hi;
+        int64_t carry = 0;
+        for (int base = 0; base < S && lo < hi; base += C::THREADS) {
+            const int r = base + tid;
+            const DtcReq q = r < S ? dtc_request(a, r) : DtcReq{0, 0, 0, 0, 0};
+            const int64_t w = dtc_work(q, hkv);
+            int64_t tot;
+            const int64_t E = carry + dtc_block_scan<C::THREADS>(w, scratch, &tot) - w;
+            int k = q.items;
+            int64_t st = 0;
+            if (q.items > 0 && E < hi && E + w > lo) {
+                k = dtc_first_from(q, hkv, lo - E, &st);
+                if (k < q.items && E + st < hi) atomicMin(found, r);
+            }
+            carry += tot;
+            __syncthreads();
+            const int f = *found;
+            if (f != INT_MAX) {
+                if (r == f) {
+                    plan_rk[0] = r;
+                    plan_rk[1] = k;
+                    plan_s[0] = E + st;
+                }
+                break;
+            }
+            if (carry >= hi) break;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int64_t range_end = plan_s[1];
+    DtcIter it0;
+    it0.r = plan_rk[0];
+    it0.k = plan_rk[1];
+    it0.s = plan_s[0];
+    if (it0.r < S) {
+        dtc_enter(a, it0, it0.r, a.cu_seqlens_q[it0.r], a.cu_seqlens_q[it0.r + 1],
+                  a.seq_lens_k[it0.r]);
+        dtc_fill(a, it0);
+    }
+    auto valid = [&](const DtcIter &x) { return x.r < S && x.s < range_end; };
+
+    if (warp >= 4 && warp < 8) {
+        // ============================================================ producers
+        // All four warps fill every stage in sequence order; warp w gathers the
+        // 8-key groups 4 w .. 4 w + 3 (32 keys) of each 128-key stage.
+        const int w = warp - 4;
+        const int krow = lane >> 4;          // row parity within each pair of key rows
+        const int sub = (lane >> 3) & 1;     // 64-dim half of a 128-dim chunk
+        const int c16 = lane & 7;            // 16-byte unit of a 128-byte row
+        const int bs = a.block_size;
+        const bool bs_pow2 = (bs & (bs - 1)) == 0;
+        const int bs_shift = __ffs(bs) - 1;
+        const uint64_t pol = policy_evict_first();   // every K/V byte is read once
+        const __nv_bfloat16 *kbase = static_cast<const __nv_bfloat16 *>(a.key_cache);
+        const __nv_bfloat16 *vbase = static_cast<const __nv_bfloat16 *>(a.value_cache);
+        // key row 8 g + 2 i + krow of a stage: its shared-memory offset within the
+        // 8-row group (128-byte swizzle: unit c16 of row k sits at c16 ^ (k & 7))
+        // and the element offset of its cache row from the group's first row
+        uint32_t soff[4];
+        int64_t kofs[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int kr = 2 * i + krow;
+            soff[i] = sub * C::SUB + kr * 128 + ((c16 ^ kr) << 4);
+            kofs[i] = (int64_t)kr * hkv * D;
+        }
+        const int eoff = sub * 64 + c16 * 8;
+        if (w == 0 && lane == 0) prefetch_tensormap(&qmap);
+        // page of this warp's 8-key group 4 w + lane (lanes 0..3) of tile jj of x
+        // (a group never crosses a page: tiles start at multiples of 8 and the
+        // block size is one too)
+        auto load_page = [&](const DtcIter &x, int jj) -> int {
+            const int kt = x.k0 + jj * C::BN;
+            const int cnt = min(C::BN, x.k1 - kt);
+            const int g = 4 * w + lane;
+            const int key0 = kt + g * 8;
+            const int blk = bs_pow2 ? key0 >> bs_shift : key0 / bs;
+            return (lane < 4 && g * 8 < cnt)
+                ? __ldg(a.block_tables + (int64_t)x.r * a.max_blocks_per_seq + blk)
+                : 0;
+        };
+        // one tile forward; itx counts the non-empty items left behind
+        auto adv = [&](DtcIter &x, int &jj, int &itx) {
+            if (++jj >= x.ntiles) {
+                jj = 0;
+                ++itx;
+                do dtc_next(a, x);
+                while (valid(x) && x.ntiles == 0);
+            }
+        };
+        // stages this warp issued but has not signalled: [pend_lo, pend_lo + npend)
+        int npend = 0, pend_lo = 0;
+        auto flush = [&]() {   // complete them all, then arrive
+            if (npend > 0) {
+                cp_async_wait<0>();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    for (int x = pend_lo; x < pend_lo + npend; ++x)
+                        mbar_arrive(bar_full + 8 * (x % C::NSLOT));
+                npend = 0;
+            }
+        };
+        int q_last[2] = {-1, -1};   // the last two items whose Q warp 4 loaded
+        // cur: the tile being issued; la: the next one (its page ids load early)
+        DtcIter cur = it0, la = it0;
+        int j = 0, itn = 0, jl = 0, itl = 0;
+        while (valid(cur) && cur.ntiles == 0) dtc_next(a, cur);
+        while (valid(la) && la.ntiles == 0) dtc_next(a, la);
+        int pg = valid(cur) ? load_page(cur, 0) : 0;
+        if (valid(la)) adv(la, jl, itl);
+        int gt = 0;
+        bool ok = true;
+        while (ok && valid(cur)) {
+            const int pgn = valid(la) ? load_page(la, jl) : 0;
+            if (j == 0 && w == 0) {   // Q^T of the item (rows = its G heads)
+                const int qb = itn & 1;
+                int bad = 0;
+                if (itn >= 2) {
+                    int ready = 0;
+                    if (lane == 0)
+                        ready = mbar_try_wait(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1);
+                    if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                        flush();   // never block while holding arrivals back
+                        if (lane == 0)
+                            bad = !mbar_wait(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1, a.err,
+                                             abort_flag);
+                    }
+                }
+                if (lane == 0 && !bad) {
+                    mbar_arrive_expect_tx(bar_q_full + 8 * qb, C::KCH * G * 128);
+#pragma unroll
+                    for (int c = 0; c < C::KCH; ++c)
+                        tma_load_3d(q_smem + qb * C::Q_BUF + c * C::NP * 128, &qmap, c * 64,
+                                    cur.h * G, (int)cur.row, bar_q_full + 8 * qb, pol);
+                }
+                if (__shfl_sync(0xffffffffu, bad, 0)) break;
+                q_last[0] = q_last[1];
+                q_last[1] = itn;
+            }
+            const int kt = cur.k0 + j * C::BN;
+            const int cnt = min(C::BN, cur.k1 - kt);
+            // element offset of the first cache row of each of this warp's groups
+            int64_t rb[4];
+#pragma unroll
+            for (int gg = 0; gg < 4; ++gg) {
+                const int page = __shfl_sync(0xffffffffu, pg, gg);
+                const int key0 = kt + (4 * w + gg) * 8;
+                const int off = bs_pow2 ? (key0 & (bs - 1)) : key0 - (key0 / bs) * bs;
+                rb[gg] = ((int64_t)(page * bs + off) * hkv + cur.h) * D;
+            }
+            for (int c = 0; c < 2 * C::KS; ++c) {   // K chunks, then V chunks
+                const int idx = gt * 2 * C::KS + c;
+                const int slot = idx % C::NSLOT;
+                const int use = idx / C::NSLOT;
+                if (use > 0) {   // this warp waited on the slot's previous use itself
+                    int ready = 0;
+                    if (lane == 0) ready = mbar_try_wait(bar_empty + 8 * slot, (use - 1) & 1);
+                    if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                        flush();   // never block while holding arrivals back
+                        int bad = 0;
+                        if (lane == 0)
+                            bad = !mbar_wait(bar_empty + 8 * slot, (use - 1) & 1, a.err,
+                                             abort_flag);
+                        if (__shfl_sync(0xffffffffu, bad, 0)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                const bool is_v = c >= C::KS;
+                const __nv_bfloat16 *src0 =
+                    (is_v ? vbase : kbase) + (is_v ? c - C::KS : c) * 128 + eoff;
+                const uint32_t dst0 = ring + slot * C::SLOT + (4 * w) * 1024;
+#pragma unroll
+                for (int gg = 0; gg < 4; ++gg)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t dst = dst0 + gg * 1024 + soff[i];
+                        if ((4 * w + gg) * 8 + 2 * i + krow < cnt)
+                            cp_async16(dst, src0 + rb[gg] + kofs[i], 16, pol);
+                        else if (is_v)   // V rows past the last key: zeros
+                            cp_async16(dst, src0, 0, pol);
+                    }
+                cp_async_commit();
+                if (npend == 0) pend_lo = idx;
+                if (++npend > C::LAG) {   // the oldest pending stage has landed: signal it
+                    cp_async_wait<C::LAG>();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_full + 8 * (pend_lo % C::NSLOT));
+                    ++pend_lo;
+                    --npend;
+                }
+            }
+            if (!ok) break;
+            ++gt;
+            adv(cur, j, itn);
+            if (valid(la)) adv(la, jl, itl);
+            pg = pgn;
+        }
+        flush();
+        // Q copies of the CTA's last two items land before the CTA can exit
+        if (w == 0 && lane == 0)
+            for (int i = 0; i < 2; ++i)
+                if (q_last[i] >= 0 && q_last[i] >= itn - 2)
+                    mbar_drain(bar_q_full + 8 * (q_last[i] & 1), (q_last[i] >> 1) & 1,
+                               kWaitLimitCycles / 8);
+    } else if (warp == 8) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16_f32(128, C::NP, 0, 0);
+            constexpr uint32_t IDESC_O = idesc_bf16_f32(128, C::NP, 1, 0);
+            // O^T[ob] (+)= V^T . P^T for global tile g_t
+            auto issue_pv = [&](int g_t, int ob, bool first, bool last) {
+                const int pb = g_t & 1;
+                mbar_wait(bar_p_full + 8 * pb, (g_t >> 1) & 1, a.err, abort_flag);
+#pragma unroll
+                for (int c = 0; c < C::KS; ++c) {
+                    const int idx = g_t * 2 * C::KS + C::KS + c;
+                    mbar_wait(bar_full + 8 * (idx % C::NSLOT), (idx / C::NSLOT) & 1, a.err,
+                              abort_flag);
+                }
+                tc_fence_after();
+                const uint32_t ps = p_smem + pb * C::P_BUF;
+#pragma unroll
+                for (int c = 0; c < C::KS; ++c) {
+                    const int idx = g_t * 2 * C::KS + C::KS + c;
+                    const uint32_t vs = ring + (idx % C::NSLOT) * C::SLOT;
+                    const uint32_t od = tmem + C::O_COL + (ob * C::KS + c) * C::NP;
+#pragma unroll
+                    for (int kk = 0; kk < C::BN / 16; ++kk) {
+                        // V^T as MN-major A: atoms of 64 dims x 8 keys; LBO steps the
+                        // 64-dim sub-chunks, SBO the 8-key groups; 16 keys per step
+                        const uint64_t ad = smem_desc_sw128(vs + kk * 16 * 128, C::SUB, 1024);
+                        const uint64_t bd =
+                            smem_desc_sw128(ps + (kk >> 2) * C::NP * 128 + (kk & 3) * 32, 16, 1024);
+                        tc_mma_bf16(od, ad, bd, IDESC_O, (!first || kk > 0) ? 1u : 0u);
+                    }
+                }
+                tc_commit(bar_o_done + 8 * pb);
+#pragma unroll
+                for (int c = 0; c < C::KS; ++c)
+                    tc_commit(bar_empty + 8 * ((g_t * 2 * C::KS + C::KS + c) % C::NSLOT));
+                if (last) tc_commit(bar_o_full + 8 * ob);
+            };
+            DtcIter cur = it0;
+            int gt = 0, itn = 0;
+            while (valid(cur)) {
+                if (cur.ntiles == 0) {
+                    dtc_next(a, cur);
+                    continue;
+                }
+                const int qb = itn & 1;
+                const int ob = itn & 1;
+                mbar_wait(bar_q_full + 8 * qb, (itn >> 1) & 1, a.err, abort_flag);
+                const uint32_t qs = q_smem + qb * C::Q_BUF;
+                for (int j = 0; j < cur.ntiles; ++j) {
+                    const int sb = gt & 1;
+                    if (gt >= 2)
+                        mbar_wait(bar_s_free + 8 * sb, ((gt >> 1) - 1) & 1, a.err, abort_flag);
+#pragma unroll
+                    for (int c = 0; c < C::KS; ++c) {
+                        const int idx = gt * 2 * C::KS + c;
+                        mbar_wait(bar_full + 8 * (idx % C::NSLOT), (idx / C::NSLOT) & 1, a.err,
+                                  abort_flag);
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < C::KS; ++c) {
+                        const uint32_t ks = ring + ((gt * 2 * C::KS + c) % C::NSLOT) * C::SLOT;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const int kg = c * 8 + kk;   // 16-dim step over the head row
+                            const uint64_t ad =
+                                smem_desc_sw128(ks + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd = smem_desc_sw128(
+                                qs + (kg >> 2) * C::NP * 128 + (kg & 3) * 32, 16, 1024);
+                            tc_mma_bf16(tmem + C::S_COL + sb * C::NP, ad, bd, IDESC_S,
+                                        kg > 0 ? 1u : 0u);
+                        }
+                    }
+                    tc_commit(bar_s_full + 8 * sb);
+#pragma unroll
+                    for (int c = 0; c < C::KS; ++c)
+                        tc_commit(bar_empty + 8 * ((gt * 2 * C::KS + c) % C::NSLOT));
+                    if (j == cur.ntiles - 1) tc_commit(bar_q_empty + 8 * qb);
+                    if (j >= 1) issue_pv(gt - 1, ob, j == 1, false);
+                    ++gt;
+                }
+                issue_pv(gt - 1, ob, cur.ntiles == 1, true);
+                ++itn;
+                dtc_next(a, cur);
+            }
+            // every MMA is finished before TMEM is freed (bounded)
+            if (gt > 0)
+                mbar_drain(bar_o_done + 8 * ((gt - 1) & 1), ((gt - 1) >> 1) & 1,
+                           kWaitLimitCycles / 8);
+        }
+    } else {
+        // ============================================================ softmax
+        const int t = tid;   // key of the tile = TMEM lane
+        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const float qsc = a.qscale;
+        const int Hq = a.num_q_heads;
+        const bool split = a.partition_size > 0;
+        DtcIter cur = it0;
+        int gt = 0, itn = 0, ie = 0;
+        while (valid(cur)) {
+            const int ob = itn & 1;
+            float m_run[G], m_ref[G], l[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                m_run[g] = -INFINITY;
+                m_ref[g] = -INFINITY;
+                l[g] = 0.f;
+            }
+            for (int j = 0; j < cur.ntiles; ++j) {
+                const int sb = gt & 1;
+                mbar_wait(bar_s_full + 8 * sb, (gt >> 1) & 1, a.err, abort_flag);
+                tc_fence_after();
+                float sv[8];
+                tmem_ld8(t_lane + C::S_COL + sb * C::NP, sv);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_s_free + 8 * sb);
+
+                const int kt = cur.k0 + j * C::BN;
+                const int cnt = min(C::BN, cur.k1 - kt);
+                const bool kv = t < cnt;
+                float x[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) x[g] = kv ? sv[g] * qsc : -INFINITY;
+                // tile max of each head across the four warps
+                float *rm = red_max + (gt & 1) * 32;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float mx = warp_max(x[g]);
+                    if (lane == 0) rm[warp * 8 + g] = mx;
+                }
+                named_barrier_sync(1, 128);
+                float mnew[G];
+                bool need[G];
+                bool any = false;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float M = fmaxf(fmaxf(rm[g], rm[8 + g]), fmaxf(rm[16 + g], rm[24 + g]));
+                    mnew[g] = fmaxf(m_run[g], M);
+                    need[g] = (mnew[g] != -INFINITY) &&
+                              (m_ref[g] == -INFINITY || mnew[g] > m_ref[g] + 8.f);
+                    any = any || need[g];
+                }
+                if (any) {   // uniform: every thread sees the same maxima
+                    float f[8];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) f[g] = 1.f;
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        if (need[g]) f[g] = m_ref[g] == -INFINITY ? 0.f : exp2f(m_ref[g] - mnew[g]);
+                    if (j >= 1) {   // O^T holds PVs of this item: rescale after the last one
+                        mbar_wait(bar_o_done + 8 * ((gt - 1) & 1), ((gt - 1) >> 1) & 1, a.err,
+                                  abort_flag);
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < C::KS; ++c) {
+                            const uint32_t oa = t_lane + C::O_COL + (ob * C::KS + c) * C::NP;
+                            float o[8];
+                            tmem_ld8(oa, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) o[e] *= f[e];
+                            tmem_st8(oa, o);
+                        }
+                        tmem_wait_st();
+                    }
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        if (need[g]) {
+                            l[g] *= f[g];
+                            m_ref[g] = mnew[g];
+                        }
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) m_run[g] = mnew[g];
+
+                // P^T buffer pb was last read by PV(gt - 2)
+                const int pb = gt & 1;
+                if (gt >= 2)
+                    mbar_wait(bar_o_done + 8 * pb, ((gt >> 1) - 1) & 1, a.err, abort_flag);
+                uint8_t *prow = smem + C::OFF_P + pb * C::P_BUF + (t >> 6) * (C::NP * 128);
+                const int kc = t & 63;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float pg =
+                        (kv && m_ref[g] != -INFINITY) ? ex2_approx(x[g] - m_ref[g]) : 0.f;
+                    l[g] += pg;
+                    *reinterpret_cast<__nv_bfloat16 *>(
+                        prow + g * 128 + ((((kc >> 3) ^ g) & 7) << 4) + (kc & 7) * 2) =
+                        __float2bfloat16_rn(pg);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_p_full + 8 * pb);
+                ++gt;
+            }
+
+            // ---- epilogue: exp-sums over the 128 keys, then O^T from TMEM
+            float L[G];
+            {
+                float *rs = red_sum + (ie & 1) * 32;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float sl = warp_sum(l[g]);
+                    if (lane == 0) rs[warp * 8 + g] = sl;
+                }
+                named_barrier_sync(1, 128);
+#pragma unroll
+                for (int g = 0; g < G; ++g) L[g] = (rs[g] + rs[8 + g]) + (rs[16 + g] + rs[24 + g]);
+            }
+            float o[C::KS][8];
+            if (cur.ntiles > 0) {
+                mbar_wait(bar_o_full + 8 * ob, (itn >> 1) & 1, a.err, abort_flag);
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < C::KS; ++c)
+                    tmem_ld8(t_lane + C::O_COL + (ob * C::KS + c) * C::NP, o[c]);
+                tmem_wait_ld();
+                tc_fence_before();
+            } else {
+#pragma unroll
+                for (int c = 0; c < C::KS; ++c)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[c][e] = 0.f;
+            }
+            const int hq0 = cur.h * G;
+            if (split) {
+                const int64_t slot0 = ((int64_t)cur.r * a.max_parts + cur.p) * Hq + hq0;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float inv = L[g] > 0.f ? 1.f / L[g] : 0.f;
+#pragma unroll
+                    for (int c = 0; c < C::KS; ++c)
+                        a.part_o[(slot0 + g) * D + c * 128 + t] = o[c][g] * inv;
+                    if (t == g) {
+                        a.part_m[slot0 + g] = m_ref[g];
+                        a.part_l[slot0 + g] = L[g];
+                    }
+                }
+            } else {
+                __nv_bfloat16 *orow =
+                    reinterpret_cast<__nv_bfloat16 *>(a.out) + (cur.row * Hq + hq0) * D;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float sc = 0.f;
+                    if (L[g] > 0.f) {
+                        if (a.sinks) {
+                            const float sk2 = a.sinks[hq0 + g] * kLog2e;
+                            const float M2 = fmaxf(m_ref[g], sk2);
+                            const float f = exp2f(m_ref[g] - M2);
+                            sc = f / (L[g] * f + exp2f(sk2 - M2));
+                        } else {
+                            sc = 1.f / L[g];
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < C::KS; ++c)
+                        orow[g * D + c * 128 + t] = __float2bfloat16_rn(o[c][g] * sc);
+                }
+            }
+            if (cur.ntiles > 0) ++itn;
+            ++ie;
+            dtc_next(a, cur);
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D, int G>
+cudaError_t launch_decode_tc_t(const CUtensorMap &qmap, const DecodeTcArgs &a, int grid,
+                               cudaStream_t stream) {
+    using C = DtcCfg<D>;
+    auto kern = paged_decode_tc_kernel<D, G>;
+    static bool configured = false;   // benign race: idempotent attribute set
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qmap, a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_decode_tc_group(int group, const CUtensorMap &qmap, const DecodeTcArgs &a,
+                                   int grid, cudaStream_t stream) {
+    switch (group) {
+        case 1: return launch_decode_tc_t<D, 1>(qmap, a, grid, stream);
+        case 2: return launch_decode_tc_t<D, 2>(qmap, a, grid, stream);
+        case 3: return launch_decode_tc_t<D, 3>(qmap, a, grid, stream);
+        case 4: return launch_decode_tc_t<D, 4>(qmap, a, grid, stream);
+        case 5: return launch_decode_tc_t<D, 5>(qmap, a, grid, stream);
+        case 6: return launch_decode_tc_t<D, 6>(qmap, a, grid, stream);
+        case 7: return launch_decode_tc_t<D, 7>(qmap, a, grid, stream);
+        case 8: return launch_decode_tc_t<D, 8>(qmap, a, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pa

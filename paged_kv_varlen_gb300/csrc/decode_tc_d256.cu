@@ -1,0 +1,12 @@
+// Instantiations of the tensor-core decode kernel for head_dim 256 (query-head
+// groups 1..8); see decode_tc.cuh.
+#include "decode_tc.cuh"
+
+namespace pa {
+
+cudaError_t launch_decode_tc_d256(int group, const CUtensorMap &qmap, const DecodeTcArgs &a,
+                                 int grid, cudaStream_t stream) {
+    return launch_decode_tc_group<256>(group, qmap, a, grid, stream);
+}
+
+}  // namespace pa

@@ -2,6 +2,7 @@
 // split-KV plan, TMA tensor maps over the page pool, and the launch sequence
 // of one attention call.  Everything here is host code except the device
 // error word.
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -174,7 +175,8 @@ PA_API const char *pa_last_error_string(void) { return g_last_error; }
 
 PA_API const char *pa_build_info(void) {
     return "libpa paged varlen attention; sm_103a; kernels: reshape_and_cache, "
-           "paged_decode (TMA ring, CUDA cores), paged_prefill_tc (tcgen05/TMEM), split_reduce";
+           "paged_decode_tc (tcgen05/TMEM, persistent), paged_decode (TMA ring, CUDA cores), "
+           "paged_prefill_tc (tcgen05/TMEM), split_reduce";
 }
 
 PA_API int pa_choose_partition_size(int num_seqs, int num_kv_heads, int max_seqlen_k,
@@ -332,10 +334,45 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
         }
     };
 
-    // 1) single-query requests (decode): (partition, kv head, request) CTAs
-    a.mode = 0;
-    cudaError_t ce = launch(dim3(max_parts, num_kv_heads, num_seqs));
-    if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode launch");
+    // 1) single-query requests (decode).  bf16 at head_dim 128 / 256: the
+    //    persistent tensor-core kernel, one CTA per SM sharing the batch's
+    //    (request, KV head, partition) items; otherwise the CUDA-core kernel,
+    //    one CTA per (partition, KV head, request).
+    cudaError_t ce;
+    if (dtype == PA_BF16 && (head_dim == 128 || head_dim == 256)) {
+        CUtensorMap qmap_d;
+        st = make_query_map(&qmap_d, q, head_dim, num_q_heads, total_q, group, 1);
+        if (st != PA_OK) return st;
+        DecodeTcArgs da;
+        da.out = out;
+        da.key_cache = key_cache;
+        da.value_cache = value_cache;
+        da.cu_seqlens_q = cu_seqlens_q;
+        da.seq_lens_k = seq_lens_k;
+        da.block_tables = block_tables;
+        da.max_blocks_per_seq = max_blocks_per_seq;
+        da.num_seqs = num_seqs;
+        da.num_q_heads = num_q_heads;
+        da.num_kv_heads = num_kv_heads;
+        da.block_size = block_size;
+        da.qscale = scale * kLog2e;
+        da.sinks = sinks;
+        da.partition_size = P;
+        da.max_parts = max_parts;
+        da.part_o = part_o;
+        da.part_m = part_m;
+        da.part_l = part_l;
+        da.err = dev.err;
+        const int64_t items_max = (int64_t)num_seqs * num_kv_heads * max_parts;
+        const int grid = (int)std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, items_max);
+        ce = head_dim == 128 ? launch_decode_tc_d128(group, qmap_d, da, grid, s)
+                             : launch_decode_tc_d256(group, qmap_d, da, grid, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode_tc launch");
+    } else {
+        a.mode = 0;
+        ce = launch(dim3(max_parts, num_kv_heads, num_seqs));
+        if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode launch");
+    }
     // 2) rows of multi-query requests (verify windows, prefill chunks): bf16 on
     //    the tensor cores, float32 on the CUDA-core row kernel
     if (max_seqlen_q > 1 && dtype == PA_BF16) {

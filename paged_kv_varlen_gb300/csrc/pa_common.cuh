@@ -90,6 +90,24 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, long l
         if (clock64() - t0 > limit) return;
 }
 
+// ---------------------------------------------------------------- cp.async
+// 16-byte asynchronous global -> shared copy (bypasses L1).  src_bytes = 0
+// reads nothing and writes 16 zero bytes.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes,
+                                           uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+                 "l"(src), "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;

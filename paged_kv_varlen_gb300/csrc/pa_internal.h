@@ -56,6 +56,29 @@ struct TcArgs {
     int *err;                  // device error word
 };
 
+// Arguments of the tensor-core kernel for single-query (decode) requests (bf16).
+struct DecodeTcArgs {
+    void *out;                 // [total_q, Hq, D] bf16
+    const void *key_cache;     // [num_blocks * block_size, Hkv, D] bf16
+    const void *value_cache;
+    const int32_t *cu_seqlens_q;
+    const int32_t *seq_lens_k;
+    const int32_t *block_tables;
+    int max_blocks_per_seq;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int block_size;
+    float qscale;              // scale * log2(e)
+    const float *sinks;        // [Hq] or nullptr
+    int partition_size;        // > 0: split partials; 0: whole range, final output
+    int max_parts;
+    float *part_o;             // [num_seqs, max_parts, Hq, D]
+    float *part_m;             // [num_seqs, max_parts, Hq]
+    float *part_l;             // [num_seqs, max_parts, Hq]
+    int *err;                  // device error word
+};
+
 // Keys per K/V tile of the tensor-core kernel and query rows per block.
 __host__ __device__ constexpr int tc_tile_keys(int head_dim) { return head_dim >= 256 ? 64 : 128; }
 __host__ __device__ constexpr int tc_block_rows(int group) { return 128 / group; }
@@ -114,6 +137,15 @@ PA_DECLARE_TC(launch_prefill_tc_d64)
 PA_DECLARE_TC(launch_prefill_tc_d128)
 PA_DECLARE_TC(launch_prefill_tc_d256)
 #undef PA_DECLARE_TC
+
+// Tensor-core kernel for single-query requests, per head_dim (bf16; 128 and
+// 256): persistent, grid.x CTAs (at most one per SM) share the batch's work.
+#define PA_DECLARE_DTC(NAME) \
+    cudaError_t NAME(int group, const CUtensorMap &qmap, const DecodeTcArgs &a, int grid, \
+                     cudaStream_t stream);
+PA_DECLARE_DTC(launch_decode_tc_d128)
+PA_DECLARE_DTC(launch_decode_tc_d256)
+#undef PA_DECLARE_DTC
 
 cudaError_t launch_reduce(int elem_bytes, int head_dim, const ReduceArgs &a, cudaStream_t stream);
 
