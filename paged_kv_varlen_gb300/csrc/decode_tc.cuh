@@ -8,7 +8,7 @@
 // partition (log2-domain reference max, exp-sum, normalised output) for the
 // shared split-KV reduce.
 //
-// GB300 design (persistent: one CTA per SM, 288 threads)
+// GB300 design (persistent: one CTA per SM, 224 threads)
 //  * A work item is (request, KV head, partition).  Every CTA scans the batch
 //    once, weighs each item by its key tiles plus one, and takes, in order,
 //    the items whose cumulative work starts inside its 1/gridDim share.
@@ -17,25 +17,23 @@
 //    serves the whole GQA group however small G is; O^T[d x 16] += V^T . P^T
 //    reads the V tile in place as an MN-major A operand.  The CUDA cores only
 //    see G scores per key instead of G * D multiply-adds.
-//  * Warps 4-7 (producers) gather the K and V tiles of all the CTA's items
-//    into one ring of 32 KB stages (128 keys x 128 dims, the tensor cores'
-//    128-byte-swizzled layout) with 16-byte cp.async copies: a 16-token page
-//    holds only 2 KB of one head's K, and TMA boxes that small are issued too
-//    slowly to reach the HBM rate from one SM.  The four warps fill every
-//    stage together, in sequence order, each a quarter of its keys; a warp
-//    signals a stage (wait_group + proxy fence, then one arrival) once it has
-//    issued LAG more, and never blocks while it holds an un-signalled stage.
-//    The page ids of the next tile and the next request's lengths are loaded
-//    a tile / a request ahead.  Rows past a tile's last key are zero-filled
-//    for V (a zero weight times a NaN pool slot would still be NaN) and left
-//    alone for K (masked).  Q comes once per item by TMA.
-//  * Warp 8 (MMA) allocates TMEM, issues S^T into one of two TMEM buffers and
+//  * Warp 4 streams the K tiles (and Q^T once per item), warp 5 the V tiles,
+//    each into its own ring of 32 KB stages (128 keys x 128 dims, the tensor
+//    cores' 128-byte-swizzled layout) by TMA, one box per run of box_rows keys
+//    of a page and 64-dim half.  A 16-token page holds only 2 KB of one head's
+//    K: one thread issuing boxes that small reaches ~26 GB/s per SM, two reach
+//    ~37.  The page ids of each tile reach shared memory by 4-byte cp.async
+//    three tiles ahead and the next request's lengths are loaded a request
+//    ahead, so the producers never wait on a load.
+//  * Warp 6 (MMA) allocates TMEM, issues S^T into one of two TMEM buffers and
 //    O^T into the accumulator of the item's parity; commits release stages.
 //  * Warps 0-3 (one thread per key = TMEM lane): scale S^T into the log2
 //    domain, take each head's tile max across the four warps, keep a
 //    reference max that moves only when the max grows by more than 2^8
 //    (then O^T and the running sums are rescaled), write P^T as bf16, and at
 //    the end of an item sum the exp-sums and write the output or the partial.
+//    Value rows past the last key of a partial tile are zeroed before the PV
+//    MMA reads them (a zero weight times a NaN pool slot would still be NaN).
 //  * Every barrier wait is bounded (pa::mbar_wait); nothing spins forever.
 #pragma once
 
@@ -55,18 +53,21 @@ struct DtcCfg {
     static constexpr int NP = 16;                  // MMA N: query heads padded to 16
     static constexpr int SLOT = BN * 256;          // ring stage: 128 keys x 128 dims bf16
     static constexpr int SUB = BN * 128;           // one 64-dim sub-chunk of a stage
-    static constexpr int NSLOT = 6;
+    static constexpr int NR = 3;                   // stages of the K ring and of the V ring
     static constexpr int Q_BUF = KCH * NP * 128;   // [KCH][16 rows][128 B]
     static constexpr int P_BUF = 2 * NP * 128;     // [2 key halves][16 rows][128 B]
-    static constexpr int OFF_Q = NSLOT * SLOT;     // two Q^T buffers
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = NR * SLOT;
+    static constexpr int OFF_Q = 2 * NR * SLOT;    // two Q^T buffers
     static constexpr int OFF_P = OFF_Q + 2 * Q_BUF;   // two P^T buffers
     static constexpr int OFF_BAR = OFF_P + 2 * P_BUF;
-    static constexpr int NBAR = 2 * NSLOT + 7 * 2;
+    static constexpr int NBAR = 4 * NR + 7 * 2;
     static constexpr int OFF_RED = OFF_BAR + NBAR * 8;   // float [2][4][8] max, [2][4][8] sum
-    static constexpr int OFF_MISC = OFF_RED + 2 * 2 * 4 * 8 * 4;
+    static constexpr int PGR = 4;                  // page-id ring of each producer (tiles)
+    static constexpr int OFF_PG = OFF_RED + 2 * 2 * 4 * 8 * 4;   // int [2 producers][PGR][16]
+    static constexpr int OFF_MISC = OFF_PG + 2 * PGR * 16 * 4;
     static constexpr int SMEM_BYTES = OFF_MISC + 128 + 1024;   // + alignment slack
-    static constexpr int THREADS = 288;            // 4 softmax + 4 producer + 1 MMA warps
-    static constexpr int LAG = 2;                  // stages a producer warp signals late
+    static constexpr int THREADS = 224;            // 4 softmax + K + V producer + MMA warps
     static constexpr int S_COL = 0;                // two S^T buffers of NP columns
     static constexpr int O_COL = 2 * NP;           // two O^T accumulators of KS * NP columns
     static constexpr int TMEM_COLS = 128;
@@ -208,20 +209,25 @@ __device__ __forceinline__ int64_t dtc_block_scan(int64_t v, long long *scratch,
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(288, 1)
-    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap, const DecodeTcArgs a) {
+__global__ void __launch_bounds__(224, 1)
+    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
+                           const __grid_constant__ CUtensorMap kmap,
+                           const __grid_constant__ CUtensorMap vmap, const DecodeTcArgs a) {
     using C = DtcCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t ring = sbase;
+    const uint32_t kring = sbase + C::OFF_K;
+    const uint32_t vring = sbase + C::OFF_V;
     const uint32_t q_smem = sbase + C::OFF_Q;
     const uint32_t p_smem = sbase + C::OFF_P;
     // barriers (each waited by its parties in order, never two phases behind)
-    const uint32_t bar_full = sbase + C::OFF_BAR;              // [NSLOT] stage loaded
-    const uint32_t bar_empty = bar_full + 8 * C::NSLOT;        // [NSLOT] stage read
-    const uint32_t bar_q_full = bar_empty + 8 * C::NSLOT;      // [2] Q^T loaded
+    const uint32_t bar_k_full = sbase + C::OFF_BAR;            // [NR] K stage loaded
+    const uint32_t bar_k_empty = bar_k_full + 8 * C::NR;       // [NR] K stage read
+    const uint32_t bar_v_full = bar_k_empty + 8 * C::NR;       // [NR] V stage loaded
+    const uint32_t bar_v_empty = bar_v_full + 8 * C::NR;       // [NR] V stage read
+    const uint32_t bar_q_full = bar_v_empty + 8 * C::NR;       // [2] Q^T loaded
     const uint32_t bar_q_empty = bar_q_full + 16;              // [2] last S^T of the item done
     const uint32_t bar_s_full = bar_q_empty + 16;              // [2] S^T in TMEM
     const uint32_t bar_s_free = bar_s_full + 16;               // [2] S^T read
@@ -230,13 +236,14 @@ __global__ void __launch_bounds__(288, 1)
     const uint32_t bar_o_full = bar_o_done + 16;               // [2] item's last PV done
     float *red_max = reinterpret_cast<float *>(smem + C::OFF_RED);   // [2][4 warps][8]
     float *red_sum = red_max + 64;                                   // [2][4 warps][8]
+    int *pgring = reinterpret_cast<int *>(smem + C::OFF_PG);         // [2][PGR][16] page ids
     uint8_t *misc = smem + C::OFF_MISC;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 8);
     int *found = reinterpret_cast<int *>(misc + 16);
     int *plan_rk = reinterpret_cast<int *>(misc + 24);               // first item: r, k
     long long *plan_s = reinterpret_cast<long long *>(misc + 32);    // its start; range end
-    long long *scratch = reinterpret_cast<long long *>(misc + 48);   // [9]
+    long long *scratch = reinterpret_cast<long long *>(misc + 48);   // [7]
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -246,9 +253,11 @@ __global__ void __launch_bounds__(288, 1)
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
-        for (int s = 0; s < C::NSLOT; ++s) {
-            mbar_init(bar_full + 8 * s, 4);    // one arrival per producer warp
-            mbar_init(bar_empty + 8 * s, 1);
+        for (int s = 0; s < C::NR; ++s) {
+            mbar_init(bar_k_full + 8 * s, 1);   // expect-tx arrival, TMA bytes
+            mbar_init(bar_k_empty + 8 * s, 1);
+            mbar_init(bar_v_full + 8 * s, 1);
+            mbar_init(bar_v_empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_q_full + 8 * b, 1);
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(288, 1)
         plan_s[0] = 0;
         plan_s[1] = 0;
     }
-    if (warp == 8) {
+    if (warp == 6) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -330,174 +339,114 @@ __global__ void __launch_bounds__(288, 1)
     }
     auto valid = [&](const DtcIter &x) { return x.r < S && x.s < range_end; };
 
-    if (warp >= 4 && warp < 8) {
-        // ============================================================ producers
-        // All four warps fill every stage in sequence order; warp w gathers the
-        // 8-key groups 4 w .. 4 w + 3 (32 keys) of each 128-key stage.
-        const int w = warp - 4;
-        const int krow = lane >> 4;          // row parity within each pair of key rows
-        const int sub = (lane >> 3) & 1;     // 64-dim half of a 128-dim chunk
-        const int c16 = lane & 7;            // 16-byte unit of a 128-byte row
-        const int bs = a.block_size;
-        const bool bs_pow2 = (bs & (bs - 1)) == 0;
-        const int bs_shift = __ffs(bs) - 1;
-        const uint64_t pol = policy_evict_first();   // every K/V byte is read once
-        const __nv_bfloat16 *kbase = static_cast<const __nv_bfloat16 *>(a.key_cache);
-        const __nv_bfloat16 *vbase = static_cast<const __nv_bfloat16 *>(a.value_cache);
-        // key row 8 g + 2 i + krow of a stage: its shared-memory offset within the
-        // 8-row group (128-byte swizzle: unit c16 of row k sits at c16 ^ (k & 7))
-        // and the element offset of its cache row from the group's first row
-        uint32_t soff[4];
-        int64_t kofs[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int kr = 2 * i + krow;
-            soff[i] = sub * C::SUB + kr * 128 + ((c16 ^ kr) << 4);
-            kofs[i] = (int64_t)kr * hkv * D;
+    // one tile forward along the sequence; itx counts the non-empty items left
+    auto adv = [&](DtcIter &x, int &jj, int &itx) {
+        if (++jj >= x.ntiles) {
+            jj = 0;
+            ++itx;
+            do dtc_next(a, x);
+            while (valid(x) && x.ntiles == 0);
         }
-        const int eoff = sub * 64 + c16 * 8;
-        if (w == 0 && lane == 0) prefetch_tensormap(&qmap);
-        // page of this warp's 8-key group 4 w + lane (lanes 0..3) of tile jj of x
-        // (a group never crosses a page: tiles start at multiples of 8 and the
-        // block size is one too)
-        auto load_page = [&](const DtcIter &x, int jj) -> int {
-            const int kt = x.k0 + jj * C::BN;
-            const int cnt = min(C::BN, x.k1 - kt);
-            const int g = 4 * w + lane;
-            const int key0 = kt + g * 8;
-            const int blk = bs_pow2 ? key0 >> bs_shift : key0 / bs;
-            return (lane < 4 && g * 8 < cnt)
-                ? __ldg(a.block_tables + (int64_t)x.r * a.max_blocks_per_seq + blk)
-                : 0;
-        };
-        // one tile forward; itx counts the non-empty items left behind
-        auto adv = [&](DtcIter &x, int &jj, int &itx) {
-            if (++jj >= x.ntiles) {
-                jj = 0;
-                ++itx;
-                do dtc_next(a, x);
-                while (valid(x) && x.ntiles == 0);
+    };
+    if (warp == 4 || warp == 5) {
+        // ============================================================ producers
+        // Warp 4 streams K (and Q^T once per item), warp 5 streams V, each into
+        // its own ring by TMA: one box per (run of box_rows keys in a page,
+        // 64-dim half).  Lanes fetch the page ids of each tile into a shared
+        // ring by 4-byte cp.async three tiles ahead, so no load is waited on.
+        const bool is_k = warp == 4;
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        const uint32_t ring0 = is_k ? kring : vring;
+        const uint32_t bfull = is_k ? bar_k_full : bar_v_full;
+        const uint32_t bempty = is_k ? bar_k_empty : bar_v_empty;
+        int *pgr = pgring + (is_k ? 0 : C::PGR * 16);
+        const int bs = a.block_size;
+        const int BR = a.box_rows;
+        const uint64_t pol = policy_evict_first();   // every K/V byte is read once
+        if (lane == 0) {
+            prefetch_tensormap(map);
+            if (is_k) prefetch_tensormap(&qmap);
+        }
+        auto fetch_pages = [&](const DtcIter &x, int jj, int t) {
+            if (valid(x)) {
+                const int kt = x.k0 + jj * C::BN;
+                const int nbox = (min(C::BN, x.k1 - kt) + BR - 1) / BR;
+                if (lane < nbox)
+                    cp_async4(smem_u32(pgr + (t % C::PGR) * 16 + lane),
+                              a.block_tables + (int64_t)x.r * a.max_blocks_per_seq +
+                                  (kt + lane * BR) / bs);
             }
+            cp_async_commit();   // one group per tile, empty or not
         };
-        // stages this warp issued but has not signalled: [pend_lo, pend_lo + npend)
-        int npend = 0, pend_lo = 0;
-        auto flush = [&]() {   // complete them all, then arrive
-            if (npend > 0) {
-                cp_async_wait<0>();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    for (int x = pend_lo; x < pend_lo + npend; ++x)
-                        mbar_arrive(bar_full + 8 * (x % C::NSLOT));
-                npend = 0;
-            }
-        };
-        int q_last[2] = {-1, -1};   // the last two items whose Q warp 4 loaded
-        // cur: the tile being issued; la: the next one (its page ids load early)
         DtcIter cur = it0, la = it0;
         int j = 0, itn = 0, jl = 0, itl = 0;
         while (valid(cur) && cur.ntiles == 0) dtc_next(a, cur);
         while (valid(la) && la.ntiles == 0) dtc_next(a, la);
-        int pg = valid(cur) ? load_page(cur, 0) : 0;
-        if (valid(la)) adv(la, jl, itl);
-        int gt = 0;
-        bool ok = true;
-        while (ok && valid(cur)) {
-            const int pgn = valid(la) ? load_page(la, jl) : 0;
-            if (j == 0 && w == 0) {   // Q^T of the item (rows = its G heads)
-                const int qb = itn & 1;
-                int bad = 0;
-                if (itn >= 2) {
-                    int ready = 0;
-                    if (lane == 0)
-                        ready = mbar_try_wait(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1);
-                    if (!__shfl_sync(0xffffffffu, ready, 0)) {
-                        flush();   // never block while holding arrivals back
-                        if (lane == 0)
-                            bad = !mbar_wait(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1, a.err,
-                                             abort_flag);
-                    }
-                }
-                if (lane == 0 && !bad) {
-                    mbar_arrive_expect_tx(bar_q_full + 8 * qb, C::KCH * G * 128);
-#pragma unroll
-                    for (int c = 0; c < C::KCH; ++c)
-                        tma_load_3d(q_smem + qb * C::Q_BUF + c * C::NP * 128, &qmap, c * 64,
-                                    cur.h * G, (int)cur.row, bar_q_full + 8 * qb, pol);
-                }
-                if (__shfl_sync(0xffffffffu, bad, 0)) break;
-                q_last[0] = q_last[1];
-                q_last[1] = itn;
-            }
-            const int kt = cur.k0 + j * C::BN;
-            const int cnt = min(C::BN, cur.k1 - kt);
-            // element offset of the first cache row of each of this warp's groups
-            int64_t rb[4];
-#pragma unroll
-            for (int gg = 0; gg < 4; ++gg) {
-                const int page = __shfl_sync(0xffffffffu, pg, gg);
-                const int key0 = kt + (4 * w + gg) * 8;
-                const int off = bs_pow2 ? (key0 & (bs - 1)) : key0 - (key0 / bs) * bs;
-                rb[gg] = ((int64_t)(page * bs + off) * hkv + cur.h) * D;
-            }
-            for (int c = 0; c < 2 * C::KS; ++c) {   // K chunks, then V chunks
-                const int idx = gt * 2 * C::KS + c;
-                const int slot = idx % C::NSLOT;
-                const int use = idx / C::NSLOT;
-                if (use > 0) {   // this warp waited on the slot's previous use itself
-                    int ready = 0;
-                    if (lane == 0) ready = mbar_try_wait(bar_empty + 8 * slot, (use - 1) & 1);
-                    if (!__shfl_sync(0xffffffffu, ready, 0)) {
-                        flush();   // never block while holding arrivals back
-                        int bad = 0;
-                        if (lane == 0)
-                            bad = !mbar_wait(bar_empty + 8 * slot, (use - 1) & 1, a.err,
-                                             abort_flag);
-                        if (__shfl_sync(0xffffffffu, bad, 0)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                }
-                const bool is_v = c >= C::KS;
-                const __nv_bfloat16 *src0 =
-                    (is_v ? vbase : kbase) + (is_v ? c - C::KS : c) * 128 + eoff;
-                const uint32_t dst0 = ring + slot * C::SLOT + (4 * w) * 1024;
-#pragma unroll
-                for (int gg = 0; gg < 4; ++gg)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t dst = dst0 + gg * 1024 + soff[i];
-                        if ((4 * w + gg) * 8 + 2 * i + krow < cnt)
-                            cp_async16(dst, src0 + rb[gg] + kofs[i], 16, pol);
-                        else if (is_v)   // V rows past the last key: zeros
-                            cp_async16(dst, src0, 0, pol);
-                    }
-                cp_async_commit();
-                if (npend == 0) pend_lo = idx;
-                if (++npend > C::LAG) {   // the oldest pending stage has landed: signal it
-                    cp_async_wait<C::LAG>();
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_full + 8 * (pend_lo % C::NSLOT));
-                    ++pend_lo;
-                    --npend;
-                }
-            }
-            if (!ok) break;
-            ++gt;
-            adv(cur, j, itn);
+        for (int t = 0; t < C::PGR - 1; ++t) {
+            fetch_pages(la, jl, t);
             if (valid(la)) adv(la, jl, itl);
-            pg = pgn;
         }
-        flush();
-        // Q copies of the CTA's last two items land before the CTA can exit
-        if (w == 0 && lane == 0)
+        int t = 0, issued = 0;
+        int q_last[2] = {-1, -1};
+        while (valid(cur)) {
+            fetch_pages(la, jl, t + C::PGR - 1);
+            if (valid(la)) adv(la, jl, itl);
+            cp_async_wait<C::PGR - 1>();   // tile t's page ids have landed
+            __syncwarp();
+            int bad = 0;
+            if (lane == 0) {
+                if (is_k && j == 0) {   // Q^T of the item, rows = its G heads
+                    const int qb = itn & 1;
+                    if (itn >= 2)
+                        bad = !mbar_wait(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1, a.err,
+                                         abort_flag);
+                    if (!bad) {
+                        mbar_arrive_expect_tx(bar_q_full + 8 * qb, C::KCH * G * 128);
+#pragma unroll
+                        for (int c = 0; c < C::KCH; ++c)
+                            tma_load_3d(q_smem + qb * C::Q_BUF + c * C::NP * 128, &qmap, c * 64,
+                                        cur.h * G, (int)cur.row, bar_q_full + 8 * qb, pol);
+                        q_last[0] = q_last[1];
+                        q_last[1] = itn;
+                    }
+                }
+                const int kt = cur.k0 + j * C::BN;
+                const int nbox = (min(C::BN, cur.k1 - kt) + BR - 1) / BR;
+                const int *pgt = pgr + (t % C::PGR) * 16;
+                for (int c = 0; c < C::KS && !bad; ++c) {   // the tile's 128-dim chunks
+                    const int idx = t * C::KS + c;
+                    const int slot = idx % C::NR;
+                    if (idx >= C::NR)
+                        bad = !mbar_wait(bempty + 8 * slot, ((idx / C::NR) - 1) & 1, a.err,
+                                         abort_flag);
+                    if (bad) break;
+                    mbar_arrive_expect_tx(bfull + 8 * slot, nbox * BR * 256);
+                    const uint32_t dst = ring0 + slot * C::SLOT;
+                    for (int u = 0; u < nbox; ++u) {
+                        const int row0 = pgt[u] * bs + (kt + u * BR) % bs;
+                        tma_load_3d(dst + u * BR * 128, map, c * 128, cur.h, row0, bfull + 8 * slot,
+                                    pol);
+                        tma_load_3d(dst + C::SUB + u * BR * 128, map, c * 128 + 64, cur.h, row0,
+                                    bfull + 8 * slot, pol);
+                    }
+                    issued = idx + 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, bad, 0)) break;
+            ++t;
+            adv(cur, j, itn);
+        }
+        cp_async_wait<0>();
+        // copies in flight land before the CTA can exit (bounded)
+        if (lane == 0) {
+            for (int i = max(0, issued - C::NR); i < issued; ++i)
+                mbar_drain(bfull + 8 * (i % C::NR), (i / C::NR) & 1, kWaitLimitCycles / 8);
             for (int i = 0; i < 2; ++i)
                 if (q_last[i] >= 0 && q_last[i] >= itn - 2)
                     mbar_drain(bar_q_full + 8 * (q_last[i] & 1), (q_last[i] >> 1) & 1,
                                kWaitLimitCycles / 8);
-    } else if (warp == 8) {
+        }
+    } else if (warp == 6) {
         // ============================================================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, C::NP, 0, 0);
@@ -508,16 +457,16 @@ __global__ void __launch_bounds__(288, 1)
                 mbar_wait(bar_p_full + 8 * pb, (g_t >> 1) & 1, a.err, abort_flag);
 #pragma unroll
                 for (int c = 0; c < C::KS; ++c) {
-                    const int idx = g_t * 2 * C::KS + C::KS + c;
-                    mbar_wait(bar_full + 8 * (idx % C::NSLOT), (idx / C::NSLOT) & 1, a.err,
+                    const int idx = g_t * C::KS + c;
+                    mbar_wait(bar_v_full + 8 * (idx % C::NR), (idx / C::NR) & 1, a.err,
                               abort_flag);
                 }
                 tc_fence_after();
                 const uint32_t ps = p_smem + pb * C::P_BUF;
 #pragma unroll
                 for (int c = 0; c < C::KS; ++c) {
-                    const int idx = g_t * 2 * C::KS + C::KS + c;
-                    const uint32_t vs = ring + (idx % C::NSLOT) * C::SLOT;
+                    const int idx = g_t * C::KS + c;
+                    const uint32_t vs = vring + (idx % C::NR) * C::SLOT;
                     const uint32_t od = tmem + C::O_COL + (ob * C::KS + c) * C::NP;
 #pragma unroll
                     for (int kk = 0; kk < C::BN / 16; ++kk) {
@@ -532,7 +481,7 @@ __global__ void __launch_bounds__(288, 1)
                 tc_commit(bar_o_done + 8 * pb);
 #pragma unroll
                 for (int c = 0; c < C::KS; ++c)
-                    tc_commit(bar_empty + 8 * ((g_t * 2 * C::KS + C::KS + c) % C::NSLOT));
+                    tc_commit(bar_v_empty + 8 * ((g_t * C::KS + c) % C::NR));
                 if (last) tc_commit(bar_o_full + 8 * ob);
             };
             DtcIter cur = it0;
@@ -552,14 +501,14 @@ __global__ void __launch_bounds__(288, 1)
                         mbar_wait(bar_s_free + 8 * sb, ((gt >> 1) - 1) & 1, a.err, abort_flag);
 #pragma unroll
                     for (int c = 0; c < C::KS; ++c) {
-                        const int idx = gt * 2 * C::KS + c;
-                        mbar_wait(bar_full + 8 * (idx % C::NSLOT), (idx / C::NSLOT) & 1, a.err,
+                        const int idx = gt * C::KS + c;
+                        mbar_wait(bar_k_full + 8 * (idx % C::NR), (idx / C::NR) & 1, a.err,
                                   abort_flag);
                     }
                     tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < C::KS; ++c) {
-                        const uint32_t ks = ring + ((gt * 2 * C::KS + c) % C::NSLOT) * C::SLOT;
+                        const uint32_t ks = kring + ((gt * C::KS + c) % C::NR) * C::SLOT;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const int kg = c * 8 + kk;   // 16-dim step over the head row
@@ -574,7 +523,7 @@ __global__ void __launch_bounds__(288, 1)
                     tc_commit(bar_s_full + 8 * sb);
 #pragma unroll
                     for (int c = 0; c < C::KS; ++c)
-                        tc_commit(bar_empty + 8 * ((gt * 2 * C::KS + c) % C::NSLOT));
+                        tc_commit(bar_k_empty + 8 * ((gt * C::KS + c) % C::NR));
                     if (j == cur.ntiles - 1) tc_commit(bar_q_empty + 8 * qb);
                     if (j >= 1) issue_pv(gt - 1, ob, j == 1, false);
                     ++gt;
@@ -675,6 +624,27 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
                 for (int g = 0; g < G; ++g) m_run[g] = mnew[g];
 
+                // value rows past the tile's last key may hold anything (pool slots
+                // past the sequence, older stages): zero them once they have landed
+                if (cnt < C::BN) {
+#pragma unroll
+                    for (int c = 0; c < C::KS; ++c) {
+                        const int idx = gt * C::KS + c;
+                        mbar_wait(bar_v_full + 8 * (idx % C::NR), (idx / C::NR) & 1, a.err,
+                                  abort_flag);
+                        if (!kv) {
+                            uint4 *r0 = reinterpret_cast<uint4 *>(
+                                smem + C::OFF_V + (idx % C::NR) * C::SLOT + t * 128);
+                            uint4 *r1 = reinterpret_cast<uint4 *>(
+                                smem + C::OFF_V + (idx % C::NR) * C::SLOT + C::SUB + t * 128);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                r0[e] = make_uint4(0, 0, 0, 0);
+                                r1[e] = make_uint4(0, 0, 0, 0);
+                            }
+                        }
+                    }
+                }
                 // P^T buffer pb was last read by PV(gt - 2)
                 const int pb = gt & 1;
                 if (gt >= 2)
@@ -769,14 +739,15 @@ __global__ void __launch_bounds__(288, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == 6) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
 template <int D, int G>
-cudaError_t launch_decode_tc_t(const CUtensorMap &qmap, const DecodeTcArgs &a, int grid,
+cudaError_t launch_decode_tc_t(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                               const CUtensorMap &vmap, const DecodeTcArgs &a, int grid,
                                cudaStream_t stream) {
     using C = DtcCfg<D>;
     auto kern = paged_decode_tc_kernel<D, G>;
@@ -787,22 +758,23 @@ cudaError_t launch_decode_tc_t(const CUtensorMap &qmap, const DecodeTcArgs &a, i
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qmap, a);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qmap, kmap, vmap, a);
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_decode_tc_group(int group, const CUtensorMap &qmap, const DecodeTcArgs &a,
-                                   int grid, cudaStream_t stream) {
+cudaError_t launch_decode_tc_group(int group, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                                   const CUtensorMap &vmap, const DecodeTcArgs &a, int grid,
+                                   cudaStream_t stream) {
     switch (group) {
-        case 1: return launch_decode_tc_t<D, 1>(qmap, a, grid, stream);
-        case 2: return launch_decode_tc_t<D, 2>(qmap, a, grid, stream);
-        case 3: return launch_decode_tc_t<D, 3>(qmap, a, grid, stream);
-        case 4: return launch_decode_tc_t<D, 4>(qmap, a, grid, stream);
-        case 5: return launch_decode_tc_t<D, 5>(qmap, a, grid, stream);
-        case 6: return launch_decode_tc_t<D, 6>(qmap, a, grid, stream);
-        case 7: return launch_decode_tc_t<D, 7>(qmap, a, grid, stream);
-        case 8: return launch_decode_tc_t<D, 8>(qmap, a, grid, stream);
+        case 1: return launch_decode_tc_t<D, 1>(qmap, kmap, vmap, a, grid, stream);
+        case 2: return launch_decode_tc_t<D, 2>(qmap, kmap, vmap, a, grid, stream);
+        case 3: return launch_decode_tc_t<D, 3>(qmap, kmap, vmap, a, grid, stream);
+        case 4: return launch_decode_tc_t<D, 4>(qmap, kmap, vmap, a, grid, stream);
+        case 5: return launch_decode_tc_t<D, 5>(qmap, kmap, vmap, a, grid, stream);
+        case 6: return launch_decode_tc_t<D, 6>(qmap, kmap, vmap, a, grid, stream);
+        case 7: return launch_decode_tc_t<D, 7>(qmap, kmap, vmap, a, grid, stream);
+        case 8: return launch_decode_tc_t<D, 8>(qmap, kmap, vmap, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

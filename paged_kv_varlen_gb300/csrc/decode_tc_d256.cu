@@ -4,9 +4,10 @@
 
 namespace pa {
 
-cudaError_t launch_decode_tc_d256(int group, const CUtensorMap &qmap, const DecodeTcArgs &a,
-                                 int grid, cudaStream_t stream) {
-    return launch_decode_tc_group<256>(group, qmap, a, grid, stream);
+cudaError_t launch_decode_tc_d256(int group, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                                 const CUtensorMap &vmap, const DecodeTcArgs &a, int grid,
+                                 cudaStream_t stream) {
+    return launch_decode_tc_group<256>(group, qmap, kmap, vmap, a, grid, stream);
 }
 
 }  // namespace pa

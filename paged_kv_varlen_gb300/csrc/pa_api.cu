@@ -340,13 +340,19 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
     //    one CTA per (partition, KV head, request).
     cudaError_t ce;
     if (dtype == PA_BF16 && (head_dim == 128 || head_dim == 256)) {
-        CUtensorMap qmap_d;
+        // box rows divide the 128-key tile, the block size and the partition
+        const int dbox = gcd_int(gcd_int(128, block_size), P > 0 ? P : 128);
+        CUtensorMap qmap_d, kmap_d, vmap_d;
         st = make_query_map(&qmap_d, q, head_dim, num_q_heads, total_q, group, 1);
+        if (st != PA_OK) return st;
+        st = make_cache_map(&kmap_d, key_cache, dtype, head_dim, num_kv_heads,
+                            num_blocks * block_size, dbox);
+        if (st != PA_OK) return st;
+        st = make_cache_map(&vmap_d, value_cache, dtype, head_dim, num_kv_heads,
+                            num_blocks * block_size, dbox);
         if (st != PA_OK) return st;
         DecodeTcArgs da;
         da.out = out;
-        da.key_cache = key_cache;
-        da.value_cache = value_cache;
         da.cu_seqlens_q = cu_seqlens_q;
         da.seq_lens_k = seq_lens_k;
         da.block_tables = block_tables;
@@ -362,11 +368,12 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
         da.part_o = part_o;
         da.part_m = part_m;
         da.part_l = part_l;
+        da.box_rows = dbox;
         da.err = dev.err;
         const int64_t items_max = (int64_t)num_seqs * num_kv_heads * max_parts;
         const int grid = (int)std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, items_max);
-        ce = head_dim == 128 ? launch_decode_tc_d128(group, qmap_d, da, grid, s)
-                             : launch_decode_tc_d256(group, qmap_d, da, grid, s);
+        ce = head_dim == 128 ? launch_decode_tc_d128(group, qmap_d, kmap_d, vmap_d, da, grid, s)
+                             : launch_decode_tc_d256(group, qmap_d, kmap_d, vmap_d, da, grid, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode_tc launch");
     } else {
         a.mode = 0;

@@ -99,6 +99,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
                  "l"(src), "r"(src_bytes), "l"(policy)
                  : "memory");
 }
+// 4-byte asynchronous global -> shared copy (through L1).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }

@@ -59,8 +59,6 @@ struct TcArgs {
 // Arguments of the tensor-core kernel for single-query (decode) requests (bf16).
 struct DecodeTcArgs {
     void *out;                 // [total_q, Hq, D] bf16
-    const void *key_cache;     // [num_blocks * block_size, Hkv, D] bf16
-    const void *value_cache;
     const int32_t *cu_seqlens_q;
     const int32_t *seq_lens_k;
     const int32_t *block_tables;
@@ -76,6 +74,7 @@ struct DecodeTcArgs {
     float *part_o;             // [num_seqs, max_parts, Hq, D]
     float *part_m;             // [num_seqs, max_parts, Hq]
     float *part_l;             // [num_seqs, max_parts, Hq]
+    int box_rows;              // rows per K/V TMA box: divides 128, the block and partition sizes
     int *err;                  // device error word
 };
 
@@ -141,7 +140,8 @@ PA_DECLARE_TC(launch_prefill_tc_d256)
 // Tensor-core kernel for single-query requests, per head_dim (bf16; 128 and
 // 256): persistent, grid.x CTAs (at most one per SM) share the batch's work.
 #define PA_DECLARE_DTC(NAME) \
-    cudaError_t NAME(int group, const CUtensorMap &qmap, const DecodeTcArgs &a, int grid, \
+    cudaError_t NAME(int group, const CUtensorMap &qmap, const CUtensorMap &kmap, \
+                     const CUtensorMap &vmap, const DecodeTcArgs &a, int grid, \
                      cudaStream_t stream);
 PA_DECLARE_DTC(launch_decode_tc_d128)
 PA_DECLARE_DTC(launch_decode_tc_d256)
