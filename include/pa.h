@@ -149,8 +149,8 @@ size_t pa_varlen_attention_workspace_size(int num_seqs, int max_seqlen_k, int nu
 
 /*
  * Partition length pa_varlen_attention uses for these sizes on a GPU with
- * `sm_count` SMs (host only): 0 = no split, else 256 or 512 (or the forced
- * value).  The library calls this with the current device's SM count.
+ * `sm_count` SMs (host only): 0 = no split, else 1024, 512 or 256 (or the
+ * forced value).  The library calls this with the current device's SM count.
  */
 int pa_choose_partition_size(int num_seqs, int num_kv_heads, int max_seqlen_k,
                              int partition_size, int sm_count);
@@ -169,7 +169,9 @@ int pa_choose_partition_size(int num_seqs, int num_kv_heads, int max_seqlen_k,
  *
  *   part_out  device float32 [num_seqs, max_parts, H_q, D]: o_p (normalised)
  *   part_max  device float32 [num_seqs, max_parts, H_q]: m_p, log2 domain
- *             (the max over the partition of scale * <q, k> * log2(e))
+ *             (a reference for the partition's scale * <q, k> * log2(e):
+ *             their max, or a value at most 8 below it, so that every
+ *             2^(t_j - m_p) stays finite)
  *   part_sum  device float32 [num_seqs, max_parts, H_q]: l_p = sum of
  *             2^(t_j - m_p) over the partition
  *   out       device [total_q, H_q, D] in `dtype`

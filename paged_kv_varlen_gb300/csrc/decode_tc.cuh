@@ -486,6 +486,8 @@ __global__ void __launch_bounds__(224, 1)
             };
             DtcIter cur = it0;
             int gt = 0, itn = 0;
+            bool pv_pending = false, pv_first = false, pv_last = false;
+            int pv_ob = 0;
             while (valid(cur)) {
                 if (cur.ntiles == 0) {
                     dtc_next(a, cur);
@@ -525,13 +527,19 @@ __global__ void __launch_bounds__(224, 1)
                     for (int c = 0; c < C::KS; ++c)
                         tc_commit(bar_k_empty + 8 * ((gt * C::KS + c) % C::NR));
                     if (j == cur.ntiles - 1) tc_commit(bar_q_empty + 8 * qb);
-                    if (j >= 1) issue_pv(gt - 1, ob, j == 1, false);
+                    // the PV of the previous tile, which may close the previous item:
+                    // S of an item's first tile never waits for the last PV before it
+                    if (pv_pending) issue_pv(gt - 1, pv_ob, pv_first, pv_last);
+                    pv_pending = true;
+                    pv_ob = ob;
+                    pv_first = j == 0;
+                    pv_last = j == cur.ntiles - 1;
                     ++gt;
                 }
-                issue_pv(gt - 1, ob, cur.ntiles == 1, true);
                 ++itn;
                 dtc_next(a, cur);
             }
+            if (pv_pending) issue_pv(gt - 1, pv_ob, pv_first, pv_last);
             // every MMA is finished before TMEM is freed (bounded)
             if (gt > 0)
                 mbar_drain(bar_o_done + 8 * ((gt - 1) & 1), ((gt - 1) >> 1) & 1,

@@ -184,12 +184,14 @@ PA_API int pa_choose_partition_size(int num_seqs, int num_kv_heads, int max_seql
     if (partition_size < 0) return 0;
     if (partition_size > 0) return partition_size;
     if (max_seqlen_k <= 512) return 0;
-    // Work budget: keep every SM busy with several CTAs of whole partitions.
-    // Long partitions first (less partial traffic), shorter when the batch is
-    // too small to fill the GPU (the page's 512-then-256 order).
+    // Work budget: keep every SM busy with several partitions.  Long
+    // partitions first (fewer partials to write and reduce, less per-partition
+    // overhead), shorter when the batch is too small to fill the GPU (the
+    // page's 512-then-256 order, with 1024 ahead of it for large batches).
     const int64_t units = (int64_t)num_seqs * num_kv_heads;
     const int64_t want = (int64_t)4 * (sm_count > 0 ? sm_count : 148);
     if (units >= want && max_seqlen_k <= 2048) return 0;
+    if (units * (max_seqlen_k / 1024) >= 2 * want) return 1024;
     if (units * (max_seqlen_k / 512) >= want) return 512;
     return 256;
 }

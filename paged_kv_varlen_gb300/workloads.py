@@ -282,7 +282,7 @@ def workload(index: int, *, partition_size: Optional[int] = None, poison: bool =
         pages = int(((n + 31) // 32).sum())
         w = build("long_decode_sinks_bf16", BF16, 24, 4, 256, 32, n - 1, np.ones(16, np.int64),
                   seed=seed, num_blocks=int(math.ceil(pages * 1.25)), with_sinks=True,
-                  partition_size=256, poison=poison, rng=rng)
+                  partition_size=0, poison=poison, rng=rng)
     else:
         raise ValueError(f"no workload {index}")
     if partition_size is not None:

@@ -63,7 +63,8 @@ def test_partition_plan(lib):
     assert f(32, 8, 8193, -1, 152) == 0         # never split
     assert f(32, 8, 8193, 512, 152) == 512      # forced
     assert f(32, 8, 300, 0, 152) == 0           # short contexts: no split
-    assert f(32, 8, 8192, 0, 152) == 512        # enough work with 512-key partitions
+    assert f(32, 8, 8192, 0, 152) == 1024       # plenty of work: long partitions
+    assert f(16, 8, 4096, 0, 152) == 512        # enough work with 512-key partitions
     assert f(2, 4, 65536, 0, 152) in (256, 512)
     assert f(1, 1, 4096, 0, 152) == 256         # tiny batch: shorter partitions
 
