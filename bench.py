@@ -429,9 +429,11 @@ def run_ours(args, rank, world, local):
                 "peak": bf16, "unit": "TFLOP/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = traffic
-    roof["kernel"] = {"decode": "paged_decode_kernel + split_reduce_kernel",
+    dec = ("paged_decode_tc_kernel" if w.dtype == "bf16" and w.head_dim in (128, 256)
+           else "paged_decode_kernel")
+    roof["kernel"] = {"decode": f"{dec} + split_reduce_kernel",
                       "prefill": "paged_prefill_tc_kernel",
-                      "mixed": "paged_decode_kernel + paged_prefill_tc_kernel + split_reduce_kernel"
+                      "mixed": f"{dec} + paged_prefill_tc_kernel + split_reduce_kernel"
                       }[kind] + " (one attention call)"
     roof["peak_source"] = (f"{peak_kind} (MEASURED_PEAKS.json "
                            f"{'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops'})"
