@@ -422,11 +422,12 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
                                                        grid, s);
             }
         };
-        // requests whose rows span two or more query blocks: CTA pairs sharing
-        // every K/V tile; virtual pairs: request r owns cu_seqlens_q[r] / (2 bq) + r ...
+        // requests whose rows span two or more query blocks: clusters of
+        // kTcCluster CTAs sharing every K/V tile; virtual cluster ids: request r
+        // owns cu_seqlens_q[r] / (kTcCluster bq) + r ...
         if (max_seqlen_q > bq) {
-            ce = launch_tc(true, dim3((unsigned)(2 * (total_q / (2 * bq) + num_seqs)),
-                                      num_kv_heads, 1));
+            const int64_t ncl = total_q / (kTcCluster * bq) + num_seqs;
+            ce = launch_tc(true, dim3((unsigned)(kTcCluster * ncl), num_kv_heads, 1));
             if (ce != cudaSuccess) return cuda_fail(ce, "paged_prefill_tc (paired) launch");
         }
         // requests whose rows fit one query block (verify windows, short chunks)

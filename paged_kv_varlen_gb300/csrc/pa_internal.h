@@ -81,6 +81,8 @@ struct DecodeTcArgs {
 // Keys per K/V tile of the tensor-core kernel and query rows per block.
 __host__ __device__ constexpr int tc_tile_keys(int head_dim) { return head_dim >= 256 ? 64 : 128; }
 __host__ __device__ constexpr int tc_block_rows(int group) { return 128 / group; }
+// CTAs of a cluster that share every K/V tile of a request (TMA multicast).
+constexpr int kTcCluster = 4;
 
 struct ReduceArgs {
     void *out;
@@ -126,8 +128,9 @@ __host__ __device__ constexpr int gcd_int(int a, int b) { return b == 0 ? a : gc
 void set_last_error(const char *msg);
 
 // Tensor-core kernel for multi-query rows, per head_dim (bf16 only).  paired:
-// clusters of two CTAs over requests with two or more query blocks (grid.x =
-// 2 * (total_q / (2 * BQ) + num_seqs)); single: one CTA per request whose rows
+// clusters of kTcCluster CTAs over requests with two or more query blocks
+// (grid.x = kTcCluster * (total_q / (kTcCluster * BQ) + num_seqs)); single:
+// one CTA per request whose rows
 // fit one block (grid.x = num_seqs).  grid.y = num_kv_heads.
 #define PA_DECLARE_TC(NAME) \
     cudaError_t NAME(int group, bool paired, const CUtensorMap &qmap, const CUtensorMap &kmap, \

@@ -7,7 +7,7 @@
 // keys, causal rows bottom-right aligned (row i sees keys j <= N - n + i),
 // with the sink logit of each head counted once in the denominator.
 //
-// GB300 design (one CTA per (request, KV head, query block), 224 threads):
+// GB300 design (one CTA per (request, KV head, query block), 352 threads):
 //  * An MMA row is a (query row, head) pair: BQ = 128 / G query rows times the
 //    G heads of one KV head fill M = 128, so every K/V page read serves the
 //    whole GQA group.  The grid walks virtual query blocks: request r owns
@@ -21,12 +21,14 @@
 //  * Warp 5 (MMA): allocates 512 TMEM columns, issues S = Q K^T into one of
 //    two TMEM buffers (so QK of tile j+1 overlaps the softmax of tile j) and
 //    O += P V with V read MN-major; commits signal mbarriers.
-//  * Warps 0-3 (softmax, one thread per TMEM lane = MMA row): load S, mask and
+//  * Warps 0-3 and 7-10 (two softmax warpgroups, one thread per TMEM lane = MMA
+//    row in each, each taking half of every tile's keys): load S, mask and
 //    scale into the log2 domain, keep a running max with lazy rescaling of O
 //    (only when the max grows by more than 2^8), write P as bf16 into one of
-//    two shared-memory buffers for the PV MMA, and finally normalise O from
-//    TMEM into the output.  The softmax waits for a PV only to reuse its P
-//    buffer (two tiles back) or to rescale O, so softmax and MMAs overlap.
+//    two TMEM buffers (the PV MMA reads its A operand from TMEM, which leaves
+//    shared memory for a third K stage), and finally normalise O from TMEM
+//    into the output.  The softmax waits for a PV only to reuse its P buffer
+//    (two tiles back) or to rescale O, so softmax and MMAs overlap.
 //  * V rows past the last key of a partial tile are zeroed before the PV MMA
 //    reads them: pool slots past the sequence may hold anything, and a
 //    zero-weight NaN would still poison the tensor-core sum.
@@ -48,33 +50,41 @@ struct TcCfg {
     // K/V tile layout [KCH][BN rows][128 B] (the tensor cores' 128-byte-swizzled
     // canonical layout), one TMA box per (page, 128-byte chunk).
     static constexpr int KV_TILE = KCH * BN * 128;
-    static constexpr int NSTAGE = D >= 128 ? 2 : 3;    // K stages (and as many V stages)
-    static constexpr int P_BYTES = (BN / 64) * 128 * 128;   // [BN/64][128 rows][128 B]
+    // K and V stages.  V is held from its load until the PV that follows the
+    // softmax, K only until its S is done, so V gets the deeper ring.
+    static constexpr int NK = D >= 256 ? 2 : (D >= 128 ? 3 : 4);
+    static constexpr int NV = D >= 128 ? 3 : 4;
     static constexpr int OFF_K = Q_BYTES;
-    static constexpr int OFF_V = OFF_K + NSTAGE * KV_TILE;
-    static constexpr int OFF_P = OFF_V + NSTAGE * KV_TILE;  // two P buffers
-    static constexpr int NBAR = 1 + 4 * NSTAGE + 2 + 2 + 2 + 2;
-    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM base, abort flag
+    static constexpr int OFF_V = OFF_K + NK * KV_TILE;
+    static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 2 + 2;
+    static constexpr int OFF_BAR = OFF_V + NV * KV_TILE;
+    static constexpr int OFF_RED = OFF_BAR + NBAR * 8;    // float [2 warpgroups][128 rows]
+    static constexpr int PGR = 4;                         // page-id ring per producer (tiles)
+    static constexpr int OFF_PG = OFF_RED + 2 * 128 * 4;  // int [2 producers][PGR][16]
+    static constexpr int OFF_MISC = OFF_PG + 2 * PGR * 16 * 4;   // TMEM base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int TMEM_COLS = 512;
     static constexpr int O_COL = 2 * BN;
-    static constexpr int THREADS = 224;                // 4 softmax + K producer + MMA + V producer
-    static_assert(O_COL + D <= TMEM_COLS, "TMEM columns");
+    static constexpr int P_COL = 2 * BN + D;           // two P buffers, BN / 2 columns each
+    // softmax warpgroup 0 (warps 0-3), K producer, MMA, V producer, softmax warpgroup 1
+    static constexpr int THREADS = 352;
+    static_assert(P_COL + BN <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(BN % 64 == 0 && D % 64 == 0, "tile shape");
 };
 
-// PAIR: a cluster of two CTAs takes two adjacent query blocks of one request
-// and KV head; both walk the same K/V tiles and each CTA loads half of every
-// tile with TMA multicast into both, halving the per-SM K/V traffic.  Without
+// PAIR: a cluster of kTcCluster CTAs takes adjacent query blocks of one
+// request and KV head; all walk the same K/V tiles and each CTA loads its
+// share of every tile's TMA boxes with multicast into all of them, dividing
+// the per-SM box issue (the gather's limit) by the cluster size.  Without
 // PAIR a CTA takes a request whose rows fit one query block.
 template <int D, int G, bool PAIR>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(352, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                             const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const TcArgs a) {
     using C = TcCfg<D, G>;
+    constexpr int CL = PAIR ? kTcCluster : 1;          // CTAs sharing each K/V tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -82,14 +92,13 @@ __global__ void __launch_bounds__(224, 1)
     const uint32_t q_smem = sbase;
     const uint32_t k_smem = sbase + C::OFF_K;
     const uint32_t v_smem = sbase + C::OFF_V;
-    const uint32_t p_smem = sbase + C::OFF_P;
     // barriers (each waited by one party in order, never two phases behind)
     const uint32_t bar_q = sbase + C::OFF_BAR;
-    const uint32_t bar_k_full = bar_q + 8;                          // [NSTAGE]
-    const uint32_t bar_k_empty = bar_k_full + 8 * C::NSTAGE;        // [NSTAGE]
-    const uint32_t bar_v_full = bar_k_empty + 8 * C::NSTAGE;        // [NSTAGE]
-    const uint32_t bar_v_empty = bar_v_full + 8 * C::NSTAGE;        // [NSTAGE]
-    const uint32_t bar_s_full = bar_v_empty + 8 * C::NSTAGE;        // [2] S buffer
+    const uint32_t bar_k_full = bar_q + 8;                          // [NK]
+    const uint32_t bar_k_empty = bar_k_full + 8 * C::NK;            // [NK]
+    const uint32_t bar_v_full = bar_k_empty + 8 * C::NK;            // [NV]
+    const uint32_t bar_v_empty = bar_v_full + 8 * C::NV;            // [NV]
+    const uint32_t bar_s_full = bar_v_empty + 8 * C::NV;            // [2] S buffer
     const uint32_t bar_s_free = bar_s_full + 16;                    // [2]
     const uint32_t bar_p_full = bar_s_free + 16;                    // [2] P buffer
     const uint32_t bar_o_done = bar_p_full + 16;                    // [2] PV of P buffer b done
@@ -106,26 +115,26 @@ __global__ void __launch_bounds__(224, 1)
     // ---------------------------------------------------------------- work item
     int r, i0, rows, kend, rot_seed;
     if (PAIR) {
-        // Virtual pair p belongs to the last request r with cu[r] / (2 BQ) + r <= p;
-        // the two CTAs of a cluster (rank 0, 1) take blocks 2l and 2l + 1.
-        const int p = blockIdx.x >> 1;
-        const int rank = blockIdx.x & 1;
+        // Virtual cluster p belongs to the last request r with
+        // cu[r] / (CL BQ) + r <= p; CTA `rank` of the cluster takes block CL l + rank.
+        const int p = blockIdx.x / CL;
+        const int rank = blockIdx.x % CL;
         int lo = 0, hi = a.num_seqs - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (a.cu_seqlens_q[mid] / (2 * C::BQ) + mid <= p) lo = mid;
+            if (a.cu_seqlens_q[mid] / (CL * C::BQ) + mid <= p) lo = mid;
             else hi = mid - 1;
         }
         r = lo;
         const int c0r = a.cu_seqlens_q[r];
         const int nr = a.cu_seqlens_q[r + 1] - c0r;
         const int nblk = (nr + C::BQ - 1) / C::BQ;
-        const int npairs = (nblk + 1) / 2;
-        const int lp = p - (c0r / (2 * C::BQ) + r);
-        if (nblk < 2 || lp < 0 || lp >= npairs) return;   // whole cluster leaves together
-        const int lpp = npairs - 1 - lp;                    // heaviest pair first
-        const int qb = 2 * lpp + rank;                      // may be past the last block
-        const int qb_hi = min(2 * lpp + 1, nblk - 1);       // the pair's heavier block
+        const int ngroups = (nblk + CL - 1) / CL;
+        const int lp = p - (c0r / (CL * C::BQ) + r);
+        if (nblk < 2 || lp < 0 || lp >= ngroups) return;  // whole cluster leaves together
+        const int lpp = ngroups - 1 - lp;                   // heaviest cluster first
+        const int qb = CL * lpp + rank;                     // may be past the last block
+        const int qb_hi = min(CL * lpp + CL - 1, nblk - 1);   // the cluster's heaviest block
         i0 = qb * C::BQ;
         rows = qb < nblk ? min(C::BQ, nr - i0) : 0;
         int Nr = a.seq_lens_k[r];
@@ -159,21 +168,23 @@ __global__ void __launch_bounds__(224, 1)
         ? (int)(((uint32_t)rot_seed * 2654435761u + (uint32_t)blockIdx.y * 40503u) % ntiles)
         : 0;
     auto tile_of = [&](int j) { const int jt = j + rot; return jt >= ntiles ? jt - ntiles : jt; };
-    constexpr uint16_t kPairMask = 0x3;
+    constexpr uint16_t kPairMask = (uint16_t)((1u << CL) - 1);   // every CTA of the cluster
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
         mbar_init(bar_q, 1);
-        for (int s = 0; s < C::NSTAGE; ++s) {
+        for (int s = 0; s < C::NK; ++s) {
             mbar_init(bar_k_full + 8 * s, 1);
-            mbar_init(bar_k_empty + 8 * s, PAIR ? 2 : 1);   // both CTAs release a stage
+            mbar_init(bar_k_empty + 8 * s, CL);   // every CTA of the cluster releases a stage
+        }
+        for (int s = 0; s < C::NV; ++s) {
             mbar_init(bar_v_full + 8 * s, 1);
-            mbar_init(bar_v_empty + 8 * s, PAIR ? 2 : 1);
+            mbar_init(bar_v_empty + 8 * s, CL);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_s_full + 8 * b, 1);
-            mbar_init(bar_s_free + 8 * b, 4);
-            mbar_init(bar_p_full + 8 * b, 4);
+            mbar_init(bar_s_free + 8 * b, 8);   // the 8 softmax warps
+            mbar_init(bar_p_full + 8 * b, 8);
             mbar_init(bar_o_done + 8 * b, 1);
         }
         fence_barrier_init();
@@ -208,6 +219,7 @@ __global__ void __launch_bounds__(224, 1)
         const uint32_t bar_full = is_k ? bar_k_full : bar_v_full;
         const uint32_t bar_empty = is_k ? bar_k_empty : bar_v_empty;
         const uint32_t stage0 = is_k ? k_smem : v_smem;
+        const int NS = is_k ? C::NK : C::NV;             // stages of this ring
         const int BR = a.box_rows;
         const uint64_t pol_kv = policy_evict_last();   // re-read by the request's other blocks
         if (lane == 0) {
@@ -223,19 +235,27 @@ __global__ void __launch_bounds__(224, 1)
             }
         }
         const int32_t *bt = a.block_tables + (int64_t)r * a.max_blocks_per_seq;
-        // page ids of a tile's boxes: lane u holds box u's page, loaded one tile ahead
-        auto pages_of = [&](int j) -> int {
-            if (j >= ntiles) return 0;
-            const int kt = tile_of(j) * C::BN;
-            const int nsub = (min(C::BN, kend - kt) + BR - 1) / BR;
-            return lane < nsub ? bt[(kt + lane * BR) / bs] : 0;
+        // page ids of tile jj's boxes reach a shared ring slot by 4-byte cp.async
+        // PGR - 1 tiles ahead (one commit group per tile), so no load is waited on
+        int *pgr = reinterpret_cast<int *>(smem + C::OFF_PG) + (is_k ? 0 : C::PGR * 16);
+        auto fetch_pages = [&](int jj) {
+            if (jj < ntiles) {
+                const int kt = tile_of(jj) * C::BN;
+                const int nsub = (min(C::BN, kend - kt) + BR - 1) / BR;
+                if (lane < nsub)
+                    cp_async4(smem_u32(pgr + (jj % C::PGR) * 16 + lane), bt + (kt + lane * BR) / bs);
+            }
+            cp_async_commit();
         };
-        int pg_cur = pages_of(0);
+        for (int jj = 0; jj < C::PGR - 1; ++jj) fetch_pages(jj);
         int issued = 0;
         for (int j = 0; j < ntiles; ++j) {
-            const int pg_next = pages_of(j + 1);
-            const int st = j % C::NSTAGE;
-            const int use = j / C::NSTAGE;
+            fetch_pages(j + C::PGR - 1);
+            cp_async_wait<C::PGR - 1>();   // tile j's page ids have landed
+            __syncwarp();
+            const int *pgt = pgr + (j % C::PGR) * 16;
+            const int st = j % NS;
+            const int use = j / NS;
             int bad = 0;
             if (lane == 0 && use > 0)
                 bad = !mbar_wait(bar_empty + 8 * st, (use - 1) & 1, a.err, abort_flag);
@@ -246,14 +266,14 @@ __global__ void __launch_bounds__(224, 1)
             if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * st, nsub * C::KCH * BR * 128);
             __syncwarp();
             const uint32_t dst = stage0 + st * C::KV_TILE;
-            // paired: rank 0 loads the first half of the boxes, rank 1 the rest,
-            // each multicast to both CTAs (every CTA expects the whole tile)
-            const int u_lo = PAIR ? ((blockIdx.x & 1) ? (nsub + 1) / 2 : 0) : 0;
-            const int u_hi = PAIR ? ((blockIdx.x & 1) ? nsub : (nsub + 1) / 2) : nsub;
-            for (int u = 0; u < nsub; ++u) {
-                const int page = __shfl_sync(0xffffffffu, pg_cur, u);
-                if (lane == 0 && u >= u_lo && u < u_hi) {
-                    const int row0 = page * bs + (kt + u * BR) % bs;
+            // cluster: CTA rk loads boxes [rk nsub / CL, (rk + 1) nsub / CL), each
+            // multicast to every CTA (every CTA expects the whole tile)
+            const int rk = (int)(blockIdx.x % CL);
+            const int u_lo = rk * nsub / CL;
+            const int u_hi = (rk + 1) * nsub / CL;
+            if (lane == 0) {
+                for (int u = u_lo; u < u_hi; ++u) {
+                    const int row0 = pgt[u] * bs + (kt + u * BR) % bs;
 #pragma unroll
                     for (int c = 0; c < C::KCH; ++c) {
                         const uint32_t d = dst + c * C::BN * 128 + u * BR * 128;
@@ -266,13 +286,13 @@ __global__ void __launch_bounds__(224, 1)
                 }
             }
             __syncwarp();
-            pg_cur = pg_next;
             issued = j + 1;
         }
+        cp_async_wait<0>();   // page-id copies in flight land before the warp leaves
         if (lane == 0) {
             if (is_k) mbar_drain(bar_q, 0, kWaitLimitCycles / 8);
-            for (int j = max(0, issued - C::NSTAGE); j < issued; ++j)
-                mbar_drain(bar_full + 8 * (j % C::NSTAGE), (j / C::NSTAGE) & 1,
+            for (int j = max(0, issued - NS); j < issued; ++j)
+                mbar_drain(bar_full + 8 * (j % NS), (j / NS) & 1,
                            kWaitLimitCycles / 8);
         }
     } else if (warp == 5) {
@@ -283,29 +303,28 @@ __global__ void __launch_bounds__(224, 1)
             mbar_wait(bar_q, 0, a.err, abort_flag);
             auto issue_pv = [&](int jj) {
                 const int pb = jj & 1;
-                const int stp = jj % C::NSTAGE;
+                const int stp = jj % C::NV;
                 mbar_wait(bar_p_full + 8 * pb, (jj >> 1) & 1, a.err, abort_flag);
-                mbar_wait(bar_v_full + 8 * stp, (jj / C::NSTAGE) & 1, a.err, abort_flag);
+                mbar_wait(bar_v_full + 8 * stp, (jj / C::NV) & 1, a.err, abort_flag);
                 tc_fence_after();
                 const uint32_t vs = v_smem + stp * C::KV_TILE;
-                const uint32_t ps = p_smem + pb * C::P_BYTES;
+                const uint32_t pt = tmem + C::P_COL + pb * (C::BN / 2);   // P in TMEM
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk) {
-                    const uint64_t ad =
-                        smem_desc_sw128(ps + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
                     // V as MN-major B: atoms of 64 d x 8 keys; LBO steps d-chunks, SBO
-                    // steps 8-key groups; one k-step is 16 keys
+                    // steps 8-key groups; one k-step is 16 keys (8 P columns)
                     const uint64_t bd = smem_desc_sw128(vs + kk * 16 * 128, C::BN * 128, 1024);
-                    tc_mma_bf16(tmem + C::O_COL, ad, bd, IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_bf16_ts(tmem + C::O_COL, pt + kk * 8, bd, IDESC_O,
+                                   (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar_o_done + 8 * pb);
                 if (PAIR) tc_commit_mc(bar_v_empty + 8 * stp, kPairMask);
                 else tc_commit(bar_v_empty + 8 * stp);
             };
             for (int j = 0; j < ntiles; ++j) {
-                const int st = j % C::NSTAGE;
+                const int st = j % C::NK;
                 const int sb = j & 1;
-                mbar_wait(bar_k_full + 8 * st, (j / C::NSTAGE) & 1, a.err, abort_flag);
+                mbar_wait(bar_k_full + 8 * st, (j / C::NK) & 1, a.err, abort_flag);
                 if (j >= 2) mbar_wait(bar_s_free + 8 * sb, ((j >> 1) - 1) & 1, a.err, abort_flag);
                 tc_fence_after();
                 const uint32_t ks = k_smem + st * C::KV_TILE;
@@ -331,25 +350,43 @@ __global__ void __launch_bounds__(224, 1)
         }
     } else {
         // ============================================================ softmax
-        const int m = tid;                                // MMA row = TMEM lane
+        // Two warpgroups share every tile: warpgroup wg takes keys
+        // [wg * BN / 2, (wg + 1) * BN / 2) of each row (TMEM lane), and half of
+        // O's columns when O is rescaled or written out.  Row maxima and sums
+        // of the two halves meet in shared memory.
+        constexpr int HB = C::BN / 2;                     // keys per warpgroup and tile
+        const int wg = warp >= 7 ? 1 : 0;
+        const int m = ((warp & 3) << 5) | lane;           // MMA row = TMEM lane
+        const int sm_tid = wg * 128 + m;                  // 0..255 over both warpgroups
+        const int kb = wg * HB;                           // first key of this half
         const int i = m / G, g = m % G;
         const bool row_ok = (m < C::M_USED) && (i < rows);
         const int qi = i0 + i;
         const int lim = min(N - 1, a.causal ? N - n + qi : N - 1);   // last visible key
         // keys up to lim_all are visible to every row of the block
         const int lim_all = min(N - 1, a.causal ? N - n + i0 : N - 1);
-        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        float *xr = reinterpret_cast<float *>(smem + C::OFF_RED);   // [2][128]
+        // the other half's value of this row (write, meet, read, meet)
+        auto exchange = [&](float v) -> float {
+            xr[wg * 128 + m] = v;
+            named_barrier_sync(1, 256);
+            const float o = xr[(1 - wg) * 128 + m];
+            named_barrier_sync(1, 256);
+            return o;
+        };
         const float qs = a.qscale;
-        float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
+        float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;   // l: this half's sum
         for (int j = 0; j < ntiles; ++j) {
             const int sb = j & 1;
             const int pb = j & 1;
-            const int st = j % C::NSTAGE;
+            const int st = j % C::NV;                     // V stage of tile j
             mbar_wait(bar_s_full + 8 * sb, (j >> 1) & 1, a.err, abort_flag);
             tc_fence_after();
-            float s[C::BN];
+            float s[HB];
 #pragma unroll
-            for (int c = 0; c < C::BN / 32; ++c) tmem_ld32(t_lane + sb * C::BN + 32 * c, s + 32 * c);
+            for (int c = 0; c < HB / 32; ++c)
+                tmem_ld32(t_lane + sb * C::BN + kb + 32 * c, s + 32 * c);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -362,24 +399,25 @@ __global__ void __launch_bounds__(224, 1)
             const bool tmask = kt0 + C::BN - 1 > lim_all;
             if (tmask) {
 #pragma unroll
-                for (int c = 0; c < C::BN; ++c)
-                    s[c] = (row_ok && kt0 + c <= lim) ? s[c] * qs : -INFINITY;
+                for (int c = 0; c < HB; ++c)
+                    s[c] = (row_ok && kt0 + kb + c <= lim) ? s[c] * qs : -INFINITY;
             }
             const float sc = tmask ? 1.f : qs;
-            // row max (8 independent chains) of sc * s, via max(s) or max(-s)
+            // max of sc * s over this half (8 independent chains), via max(s) or max(-s)
             const bool neg = sc < 0.f;
             float mx[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) mx[k] = neg ? -s[k] : s[k];
 #pragma unroll
-            for (int c = 8; c < C::BN; c += 8)
+            for (int c = 8; c < HB; c += 8)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], neg ? -s[c + k] : s[c + k]);
 #pragma unroll
             for (int k = 4; k > 0; k >>= 1)
 #pragma unroll
                 for (int q = 0; q < k; ++q) mx[q] = fmaxf(mx[q], mx[q + k]);
-            const float tmax = mx[0] == -INFINITY ? -INFINITY : mx[0] * fabsf(sc);
+            const float hmax = mx[0] == -INFINITY ? -INFINITY : mx[0] * fabsf(sc);
+            const float tmax = fmaxf(hmax, exchange(hmax));   // the whole row's tile max
             const float m_new = fmaxf(m_run, tmax);
             m_run = m_new;
             const bool need = (m_new != -INFINITY) && (m_ref == -INFINITY || m_new > m_ref + 8.f);
@@ -388,29 +426,31 @@ __global__ void __launch_bounds__(224, 1)
             // before the PV MMA (a zero weight times NaN is still NaN).
             const int cnt = min(C::BN, kend - kt0);
             if (cnt < C::BN) {
-                mbar_wait(bar_v_full + 8 * st, (j / C::NSTAGE) & 1, a.err, abort_flag);
+                mbar_wait(bar_v_full + 8 * st, (j / C::NV) & 1, a.err, abort_flag);
                 uint8_t *vsp = smem + C::OFF_V + st * C::KV_TILE;
                 const int nchunk = (C::BN - cnt) * C::KCH * 8;   // 16-byte pieces to clear
-                for (int q = tid; q < nchunk; q += 128) {
+                for (int q = sm_tid; q < nchunk; q += 256) {
                     const int k = cnt + q / (C::KCH * 8);          // key row of the tile
                     const int c = (q >> 3) % C::KCH;               // 128-byte chunk of the row
                     const int off = c * C::BN * 128 + k * 128;
                     *reinterpret_cast<uint4 *>(vsp + off + (q & 7) * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
-            // O changes only when a row's reference max moves: then PV(j-1) must be done.
+            // O changes only when a row's reference max moves: then PV(j-1) must be
+            // done.  Each warpgroup rescales its half of O's columns.
             if (j >= 1 && __any_sync(0xffffffffu, need)) {
                 mbar_wait(bar_o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, a.err, abort_flag);
                 tc_fence_after();
                 const float f = need ? (m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new)) : 1.f;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     float o[32];
-                    tmem_ld32(t_lane + C::O_COL + 32 * c, o);
+                    const uint32_t oa = t_lane + C::O_COL + wg * (D / 2) + 32 * c;
+                    tmem_ld32(oa, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= f;
-                    tmem_st32(t_lane + C::O_COL + 32 * c, o);
+                    tmem_st32(oa, o);
                 }
                 tmem_wait_st();
             }
@@ -420,63 +460,63 @@ __global__ void __launch_bounds__(224, 1)
             }
             // P buffer pb was last read by PV(j-2)
             if (j >= 2) mbar_wait(bar_o_done + 8 * pb, ((j >> 1) - 1) & 1, a.err, abort_flag);
-            // P = 2^(sc * s - m_ref) as bf16 (masked keys: 2^-inf = 0),
-            // row m of the K-major 128-byte-swizzled A tile
+            // P = 2^(sc * s - m_ref) as bf16 (masked keys: 2^-inf = 0) into this
+            // row's TMEM lane, two keys per 32-bit column: the A operand of PV
             const float2 qs2 = make_float2(sc, sc);
             const float mu = (m_ref == -INFINITY) ? 0.f : -m_ref;
             const float2 mu2 = make_float2(mu, mu);
             float2 sum2[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) sum2[k] = make_float2(0.f, 0.f);
-            const uint32_t ps = p_smem + pb * C::P_BYTES;
+            const uint32_t pt = t_lane + C::P_COL + pb * (C::BN / 2) + kb / 2;
 #pragma unroll
-            for (int k8 = 0; k8 < C::BN / 8; ++k8) {
-                uint32_t w4[4];
+            for (int k16 = 0; k16 < HB / 16; ++k16) {
+                uint32_t w8[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float2 x = __ffma2_rn(make_float2(s[k8 * 8 + 2 * e], s[k8 * 8 + 2 * e + 1]),
+                for (int e = 0; e < 8; ++e) {
+                    float2 x = __ffma2_rn(make_float2(s[k16 * 16 + 2 * e], s[k16 * 16 + 2 * e + 1]),
                                           qs2, mu2);
                     x.x = ex2_approx(x.x);
                     x.y = ex2_approx(x.y);
-                    sum2[e] = __fadd2_rn(sum2[e], x);
-                    w4[e] = pack_bf16x2(x.x, x.y);
+                    sum2[e & 3] = __fadd2_rn(sum2[e & 3], x);
+                    w8[e] = pack_bf16x2(x.x, x.y);
                 }
-                const uint32_t addr = ps + (k8 >> 3) * 128 * 128 + m * 128 +
-                                      (((k8 & 7) ^ (m & 7)) << 4);
-                sts128(addr, w4[0], w4[1], w4[2], w4[3]);
+                tmem_st8u(pt + k16 * 8, w8);
             }
             const float2 sa = __fadd2_rn(sum2[0], sum2[1]);
             const float2 sbb = __fadd2_rn(sum2[2], sum2[3]);
             l += (sa.x + sa.y) + (sbb.x + sbb.y);
-            fence_proxy_async_smem();
+            tmem_wait_st();
+            fence_proxy_async_smem();   // zeroed V rows (generic writes) reach the tensor core
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_p_full + 8 * pb);
         }
-        // ---- epilogue: out = O / (l + sink term)
+        // ---- epilogue: out = O / (l + sink term); each warpgroup writes half of D
         if (ntiles > 0) {
             mbar_wait(bar_o_done + 8 * ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, a.err,
                       abort_flag);
             tc_fence_after();
         }
+        const float l_row = l + exchange(l);
         float scale_out = 0.f;
-        if (l > 0.f) {
+        if (l_row > 0.f) {
             if (a.sinks) {
                 const float sk2 = a.sinks[h * G + g] * kLog2e;
                 const float M2 = fmaxf(m_ref, sk2);
                 const float f = exp2f(m_ref - M2);
-                scale_out = f / (l * f + exp2f(sk2 - M2));
+                scale_out = f / (l_row * f + exp2f(sk2 - M2));
             } else {
-                scale_out = 1.f / l;
+                scale_out = 1.f / l_row;
             }
         }
         __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(a.out) +
-                              ((row_base + i) * Hq + (int64_t)h * G + g) * D;
+                              ((row_base + i) * Hq + (int64_t)h * G + g) * D + wg * (D / 2);
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
             float o[32];
             if (ntiles > 0) {
-                tmem_ld32(t_lane + C::O_COL + 32 * c, o);
+                tmem_ld32(t_lane + C::O_COL + wg * (D / 2) + 32 * c, o);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -531,7 +571,7 @@ cudaError_t launch_prefill_tc_t(const CUtensorMap &qmap, const CUtensorMap &kmap
     cudaLaunchAttribute attr[1];
     if (PAIR) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = kTcCluster;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
