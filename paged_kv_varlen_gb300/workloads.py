@@ -290,6 +290,22 @@ def workload(index: int, *, partition_size: Optional[int] = None, poison: bool =
     return w
 
 
+def padded(w: Workload, *, seed: int = 7) -> Workload:
+    """The same batch laid out padded instead of packed: every request gets
+    max(q) query rows and max(N) keys (prior = max(N) - max(q)), the shape a
+    padded [B, H, T_max, D] attention computes on.  The rows and keys past a
+    request's own lengths are padding: the work they cost is the price of not
+    packing (aisignalhub.me, "packed queries and paged KV": batch A vs B)."""
+    S = w.num_seqs
+    qmax = int(w.q_lens.max())
+    nmax = int(w.seq_lens.max())
+    pages = S * ((nmax + w.block_size - 1) // w.block_size)
+    return build(w.name + "_padded", w.dtype, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                 w.block_size, np.full(S, nmax - qmax, np.int64), np.full(S, qmax, np.int64),
+                 seed=seed, num_blocks=int(math.ceil(pages * 1.1)) + 1, causal=w.causal,
+                 with_sinks=w.sinks is not None, partition_size=w.partition_size)
+
+
 def random_small(seed: int, *, dtype: str = BF16, num_seqs: int = 3, num_q_heads: int = 4,
                  num_kv_heads: int = 2, head_dim: int = 64, block_size: int = 16,
                  max_prior: int = 70, max_q: int = 5, causal: bool = True,

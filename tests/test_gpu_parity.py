@@ -127,6 +127,27 @@ def test_block_size_translation_is_invisible():
     assert torch.equal(base.view(torch.int16), out.view(torch.int16))
 
 
+def test_block_size_144_as_nine_16_token_pages():
+    """A 144-token-page pool (the page size of hybrid models) attended directly and
+    viewed as nine 16-token pages by a reshape and a block-table expansion
+    (pptc.cn, block-size translation): parity with the oracle, identical bits."""
+    w = wl.random_small(83, dtype=wl.BF16, num_seqs=4, block_size=144, max_prior=700, max_q=4)
+    check_step(w)
+    dw = _run(w)
+    base = dw.out.clone()
+    kc16 = dw.key_cache.view(w.num_blocks * 9, 16, w.num_kv_heads, w.head_dim)
+    vc16 = dw.value_cache.view(w.num_blocks * 9, 16, w.num_kv_heads, w.head_dim)
+    bt = torch.from_numpy(w.block_tables).cuda()
+    bt16 = torch.stack([bt * 9 + k for k in range(9)], dim=2).reshape(bt.shape[0], -1)
+    bt16 = torch.where(bt16 >= 0, bt16, torch.full_like(bt16, -1)).to(torch.int32).contiguous()
+    out = torch.empty_like(base)
+    pa.pa_varlen_attention(out, dw.q, kc16, vc16, dw.cu_seqlens_q, dw.seq_lens_k, bt16,
+                           max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k,
+                           scale=w.scale, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(base.view(torch.int16), out.view(torch.int16))
+
+
 def test_packing_independence():
     w = wl.random_small(83, dtype=wl.F32, num_seqs=4, max_prior=300, max_q=6)
     packed = from_dev(_run(w).out)
