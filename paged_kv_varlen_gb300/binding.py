@@ -54,6 +54,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pa_varlen_attention_workspace_size.argtypes = [I, I, I, I, I]
     lib.pa_choose_partition_size.restype = I
     lib.pa_choose_partition_size.argtypes = [I, I, I, I, I]
+    lib.pa_scatter_and_attend.restype = I
+    lib.pa_scatter_and_attend.argtypes = [P, P, L, P, L, P, P, P, P, P, P, P, I, I, L, I, I, I, I,
+                                          I, I, L, F, P, I, I, P, S, I, P]
     lib.pa_split_kv_reduce.restype = I
     lib.pa_split_kv_reduce.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P]
     lib.pa_device_error.restype = I
@@ -155,6 +158,44 @@ def pa_varlen_attention(out: torch.Tensor, q: torch.Tensor, key_cache: torch.Ten
                                  _ptr(sinks), int(bool(causal)), int(partition_size),
                                  _ptr(workspace), workspace.numel(), _dtype(q), _stream(stream))
     _check(st, "pa_varlen_attention")
+    return out
+
+
+def pa_scatter_and_attend(new_k: torch.Tensor, new_v: torch.Tensor, slot_mapping: torch.Tensor,
+                          out: torch.Tensor, q: torch.Tensor, key_cache: torch.Tensor,
+                          value_cache: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                          seq_lens_k: torch.Tensor, block_tables: torch.Tensor, *,
+                          max_seqlen_q: int, max_seqlen_k: int, scale: float,
+                          sinks: Optional[torch.Tensor] = None, causal: bool = True,
+                          partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """pa_reshape_and_cache(new_k, new_v, ...) then pa_varlen_attention(...) as one
+    call; new_k/new_v [total_q, H_kv, D] (rows may be strided), slot_mapping int64."""
+    lib = load_library()
+    total_q, Hq, D = q.shape
+    nb, bs, Hkv, _ = key_cache.shape
+    S = seq_lens_k.shape[0]
+    if new_k.stride() != new_v.stride() or new_k.stride(2) != 1 or new_k.stride(1) != D:
+        raise PAError("new_k/new_v rows must be [H_kv, D]-contiguous with equal strides")
+    if slot_mapping.dtype != torch.int64:
+        raise PAError("slot_mapping must be int64")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("seq_lens_k", seq_lens_k),
+                    ("block_tables", block_tables)):
+        if t.dtype != torch.int32:
+            raise PAError(f"{name} must be int32")
+    if sinks is not None and sinks.dtype != torch.float32:
+        raise PAError("sinks must be float32")
+    if workspace is None:
+        nbytes = pa_varlen_attention_workspace_size(S, max_seqlen_k, Hq, D, partition_size)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    st = lib.pa_scatter_and_attend(
+        ctypes.c_void_p(new_k.data_ptr()), ctypes.c_void_p(new_v.data_ptr()), new_k.stride(0),
+        _ptr(slot_mapping), new_k.shape[0], _ptr(out), _ptr(q), _ptr(key_cache),
+        _ptr(value_cache), _ptr(cu_seqlens_q), _ptr(seq_lens_k), _ptr(block_tables),
+        block_tables.shape[1], S, total_q, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, bs,
+        nb, float(scale), _ptr(sinks), int(bool(causal)), int(partition_size), _ptr(workspace),
+        workspace.numel(), _dtype(q), _stream(stream))
+    _check(st, "pa_scatter_and_attend")
     return out
 
 

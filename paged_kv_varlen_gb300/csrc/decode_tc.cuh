@@ -34,6 +34,11 @@
 //    the end of an item sum the exp-sums and write the output or the partial.
 //    Value rows past the last key of a partial tile are zeroed before the PV
 //    MMA reads them (a zero weight times a NaN pool slot would still be NaN).
+//  * Fused scatter (pa_scatter_and_attend): the producer that loads a decode
+//    request's last tile first writes that request's newest K (V) row for its
+//    KV head into the cache and fences it for TMA; the softmax warps scatter,
+//    while the pipeline fills, every row no decode item reads (rows of the
+//    multi-query requests, whose kernel runs after this one).
 //  * Every barrier wait is bounded (pa::mbar_wait); nothing spins forever.
 #pragma once
 
@@ -84,17 +89,20 @@ struct DtcReq {
     int N;       // keys
     int wfull;   // work of an item of a full partition
     int wlast;   // work of an item of the last partition
+    int whole;   // the items reach the request's last key (its newest token)
 };
 
 // c0, c1 = cu_seqlens_q[r], cu_seqlens_q[r + 1]; sl = seq_lens_k[r]
 __device__ __forceinline__ DtcReq dtc_request_from(const DecodeTcArgs &a, int c0, int c1, int sl) {
-    DtcReq q = {0, 0, 0, 0, 0};
+    DtcReq q = {0, 0, 0, 0, 0, 0};
     if (c1 - c0 != 1) return q;                       // multi-query request: other kernel
     int N = max(0, min(sl, a.max_blocks_per_seq * a.block_size));
     q.N = N;
+    q.whole = N >= 1 && min(sl, a.max_blocks_per_seq * a.block_size) == sl;
     const int P = a.partition_size;
     if (P > 0) {
         // partials exist for max_parts partitions only (the reduce reads no more)
+        if (N > a.max_parts * P) q.whole = 0;
         N = min(N, a.max_parts * P);
         q.N = N;
         q.np = (N + P - 1) / P;
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(224, 1)
         int64_t carry = 0;
         for (int base = 0; base < S && lo < hi; base += C::THREADS) {
             const int r = base + tid;
-            const DtcReq q = r < S ? dtc_request(a, r) : DtcReq{0, 0, 0, 0, 0};
+            const DtcReq q = r < S ? dtc_request(a, r) : DtcReq{0, 0, 0, 0, 0, 0};
             const int64_t w = dtc_work(q, hkv);
             int64_t tot;
             const int64_t E = carry + dtc_block_scan<C::THREADS>(w, scratch, &tot) - w;
@@ -393,6 +401,22 @@ __global__ void __launch_bounds__(224, 1)
             if (valid(la)) adv(la, jl, itl);
             cp_async_wait<C::PGR - 1>();   // tile t's page ids have landed
             __syncwarp();
+            if (a.new_k != nullptr && cur.q.whole && cur.k1 == cur.q.N && j == cur.ntiles - 1) {
+                // fused scatter: this step's row of the request is its last key,
+                // which this tile reads; write it first (K here, V in warp 5)
+                const int64_t slot = a.slot_mapping[cur.row];
+                if (slot >= 0 && slot < a.num_slots) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        static_cast<const __nv_bfloat16 *>(is_k ? a.new_k : a.new_v) +
+                        cur.row * a.new_stride + (int64_t)cur.h * D);
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        static_cast<__nv_bfloat16 *>(is_k ? a.key_cache : a.value_cache) +
+                        (slot * hkv + cur.h) * D);
+                    for (int e = lane; e < D / 8; e += 32) dst[e] = src[e];
+                    fence_proxy_async_global();   // before this warp's TMA reads it
+                }
+                __syncwarp();
+            }
             int bad = 0;
             if (lane == 0) {
                 if (is_k && j == 0) {   // Q^T of the item, rows = its G heads
@@ -552,6 +576,30 @@ __global__ void __launch_bounds__(224, 1)
         const float qsc = a.qscale;
         const int Hq = a.num_q_heads;
         const bool split = a.partition_size > 0;
+        if (a.new_k != nullptr) {
+            // Fused scatter of every row no decode item writes (rows of multi-query
+            // requests, whose kernel runs after this one; rows whose slot lies
+            // past what the items read): one row per thread, all heads.
+            const int64_t rowv = (int64_t)hkv * D / 8;   // 16-byte pieces per row
+            for (int64_t t = (int64_t)blockIdx.x * 128 + tid; t < a.total_q;
+                 t += (int64_t)gridDim.x * 128) {
+                const int r = request_of_row(a.cu_seqlens_q, S, t);
+                const DtcReq q = dtc_request(a, r);
+                if (q.items > 0 && q.whole) continue;   // written by its item's producers
+                const int64_t slot = a.slot_mapping[t];
+                if (slot < 0 || slot >= a.num_slots) continue;
+                const uint4 *sk = reinterpret_cast<const uint4 *>(
+                    static_cast<const __nv_bfloat16 *>(a.new_k) + t * a.new_stride);
+                const uint4 *sv = reinterpret_cast<const uint4 *>(
+                    static_cast<const __nv_bfloat16 *>(a.new_v) + t * a.new_stride);
+                uint4 *dk = reinterpret_cast<uint4 *>(a.key_cache) + slot * rowv;
+                uint4 *dv = reinterpret_cast<uint4 *>(a.value_cache) + slot * rowv;
+                for (int64_t e = 0; e < rowv; ++e) {
+                    dk[e] = sk[e];
+                    dv[e] = sv[e];
+                }
+            }
+        }
         DtcIter cur = it0;
         int gt = 0, itn = 0, ie = 0;
         while (valid(cur)) {

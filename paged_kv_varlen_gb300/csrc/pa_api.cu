@@ -150,6 +150,14 @@ SplitLayout split_layout(int num_seqs, int max_parts, int num_q_heads, int head_
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// This step's K/V rows for pa_scatter_and_attend (one per query row).
+struct FusedScatter {
+    const void *key;
+    const void *value;
+    int64_t stride;                 // elements between tokens
+    const int64_t *slot_mapping;
+};
+
 }  // namespace
 
 // Lets other translation units of the library report a message through
@@ -231,15 +239,17 @@ PA_API pa_status pa_reshape_and_cache(const void *key, const void *value, int64_
     return PA_OK;
 }
 
-PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_cache,
-                                     const void *value_cache, const int32_t *cu_seqlens_q,
-                                     const int32_t *seq_lens_k, const int32_t *block_tables,
-                                     int max_blocks_per_seq, int num_seqs, int64_t total_q,
-                                     int max_seqlen_q, int max_seqlen_k, int num_q_heads,
-                                     int num_kv_heads, int head_dim, int block_size,
-                                     int64_t num_blocks, float scale, const float *sinks,
-                                     int causal, int partition_size, void *workspace,
-                                     size_t workspace_bytes, pa_dtype dtype, void *stream) {
+// The attention call; with `fs`, this step's K/V rows are scattered first --
+// inside the tensor-core decode kernel when it runs, else by the scatter kernel.
+static pa_status attention_impl(void *out, const void *q, const void *key_cache,
+                                const void *value_cache, const int32_t *cu_seqlens_q,
+                                const int32_t *seq_lens_k, const int32_t *block_tables,
+                                int max_blocks_per_seq, int num_seqs, int64_t total_q,
+                                int max_seqlen_q, int max_seqlen_k, int num_q_heads,
+                                int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                float scale, const float *sinks, int causal, int partition_size,
+                                void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                                void *stream, const FusedScatter *fs) {
     // ---- host-side checks (nothing is launched if one fails)
     if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
     if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
@@ -336,12 +346,26 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
         }
     };
 
+    // 0) this step's K/V rows (pa_scatter_and_attend): fused into the tensor-core
+    //    decode kernel when it runs and the rows are 16-byte aligned, else the
+    //    scatter kernel first
+    const bool tc_decode = dtype == PA_BF16 && (head_dim == 128 || head_dim == 256);
+    const bool fuse = fs && tc_decode && aligned16(fs->key) && aligned16(fs->value) &&
+                      (fs->stride * 2) % 16 == 0;
+    cudaError_t ce;
+    if (fs && !fuse) {
+        const int64_t eb = dtype == PA_F32 ? 4 : 2;
+        ce = launch_reshape_and_cache(fs->key, fs->value, fs->stride * eb, const_cast<void *>(key_cache),
+                                      const_cast<void *>(value_cache), fs->slot_mapping, total_q,
+                                      (int64_t)num_kv_heads * head_dim * eb,
+                                      num_blocks * block_size, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "reshape_and_cache launch");
+    }
     // 1) single-query requests (decode).  bf16 at head_dim 128 / 256: the
     //    persistent tensor-core kernel, one CTA per SM sharing the batch's
     //    (request, KV head, partition) items; otherwise the CUDA-core kernel,
     //    one CTA per (partition, KV head, request).
-    cudaError_t ce;
-    if (dtype == PA_BF16 && (head_dim == 128 || head_dim == 256)) {
+    if (tc_decode) {
         // box rows divide the 128-key tile, the block size and the partition
         const int dbox = gcd_int(gcd_int(128, block_size), P > 0 ? P : 128);
         CUtensorMap qmap_d, kmap_d, vmap_d;
@@ -372,8 +396,20 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
         da.part_l = part_l;
         da.box_rows = dbox;
         da.err = dev.err;
+        da.new_k = fuse ? fs->key : nullptr;
+        da.new_v = fuse ? fs->value : nullptr;
+        da.new_stride = fuse ? fs->stride : 0;
+        da.slot_mapping = fuse ? fs->slot_mapping : nullptr;
+        da.key_cache = const_cast<void *>(key_cache);
+        da.value_cache = const_cast<void *>(value_cache);
+        da.num_slots = num_blocks * block_size;
+        da.total_q = total_q;
         const int64_t items_max = (int64_t)num_seqs * num_kv_heads * max_parts;
-        const int grid = (int)std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, items_max);
+        // (a fused scatter needs the kernel even with no decode rows)
+        const int grid = (int)std::max<int64_t>(
+            1, std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148,
+                                 fuse ? std::max<int64_t>(items_max, (total_q + 127) / 128)
+                                      : items_max));
         ce = head_dim == 128 ? launch_decode_tc_d128(group, qmap_d, kmap_d, vmap_d, da, grid, s)
                              : launch_decode_tc_d256(group, qmap_d, kmap_d, vmap_d, da, grid, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode_tc launch");
@@ -456,6 +492,50 @@ PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_c
         if (ce != cudaSuccess) return cuda_fail(ce, "split_reduce launch");
     }
     return PA_OK;
+}
+
+PA_API pa_status pa_varlen_attention(void *out, const void *q, const void *key_cache,
+                                     const void *value_cache, const int32_t *cu_seqlens_q,
+                                     const int32_t *seq_lens_k, const int32_t *block_tables,
+                                     int max_blocks_per_seq, int num_seqs, int64_t total_q,
+                                     int max_seqlen_q, int max_seqlen_k, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int block_size,
+                                     int64_t num_blocks, float scale, const float *sinks,
+                                     int causal, int partition_size, void *workspace,
+                                     size_t workspace_bytes, pa_dtype dtype, void *stream) {
+    return attention_impl(out, q, key_cache, value_cache, cu_seqlens_q, seq_lens_k, block_tables,
+                          max_blocks_per_seq, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                          sinks, causal, partition_size, workspace, workspace_bytes, dtype,
+                          stream, nullptr);
+}
+
+PA_API pa_status pa_scatter_and_attend(const void *key, const void *value, int64_t kv_token_stride,
+                                       const int64_t *slot_mapping, int64_t num_tokens, void *out,
+                                       const void *q, void *key_cache, void *value_cache,
+                                       const int32_t *cu_seqlens_q, const int32_t *seq_lens_k,
+                                       const int32_t *block_tables, int max_blocks_per_seq,
+                                       int num_seqs, int64_t total_q, int max_seqlen_q,
+                                       int max_seqlen_k, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int64_t num_blocks,
+                                       float scale, const float *sinks, int causal,
+                                       int partition_size, void *workspace,
+                                       size_t workspace_bytes, pa_dtype dtype, void *stream) {
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (num_tokens != total_q || num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (num_kv_heads <= 0 || head_dim <= 0 ||
+        kv_token_stride < (int64_t)num_kv_heads * head_dim)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!key || !value || !slot_mapping)) return PA_ERR_INVALID_ARG;
+    const uintptr_t e = dtype == PA_F32 ? 4 : 2;
+    if (((reinterpret_cast<uintptr_t>(key) | reinterpret_cast<uintptr_t>(value)) % e) != 0)
+        return PA_ERR_INVALID_ARG;
+    const FusedScatter fs = {key, value, kv_token_stride, slot_mapping};
+    return attention_impl(out, q, key_cache, value_cache, cu_seqlens_q, seq_lens_k, block_tables,
+                          max_blocks_per_seq, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                          sinks, causal, partition_size, workspace, workspace_bytes, dtype,
+                          stream, &fs);
 }
 
 PA_API pa_status pa_split_kv_reduce(void *out, const float *part_out, const float *part_max,

@@ -90,6 +90,12 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, long l
         if (clock64() - t0 > limit) return;
 }
 
+// Generic-proxy writes to global memory made visible to later async-proxy
+// (TMA) reads of the same addresses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte asynchronous global -> shared copy (bypasses L1).  src_bytes = 0
 // reads nothing and writes 16 zero bytes.

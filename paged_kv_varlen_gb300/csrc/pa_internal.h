@@ -76,6 +76,16 @@ struct DecodeTcArgs {
     float *part_l;             // [num_seqs, max_parts, Hq]
     int box_rows;              // rows per K/V TMA box: divides 128, the block and partition sizes
     int *err;                  // device error word
+    // Fused scatter (pa_scatter_and_attend; new_k == nullptr: none): this
+    // step's K/V row of every query row t goes to slot slot_mapping[t].
+    const void *new_k;         // [total_q, Hkv, D] bf16 rows, new_stride elements apart
+    const void *new_v;
+    int64_t new_stride;
+    const int64_t *slot_mapping;
+    void *key_cache;           // [num_slots, Hkv, D] bf16 (the caches the kernel reads)
+    void *value_cache;
+    int64_t num_slots;         // num_blocks * block_size
+    int64_t total_q;
 };
 
 // Keys per K/V tile of the tensor-core kernel and query rows per block.

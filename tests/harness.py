@@ -77,6 +77,18 @@ class DeviceWorkload:
         self.scatter()
         return self.attention(**kw)
 
+    def fused_step(self, partition_size=None, out=None):
+        """The same step through pa_scatter_and_attend (one call)."""
+        w = self.w
+        out = self.out if out is None else out
+        pa.pa_scatter_and_attend(
+            self.new_k, self.new_v, self.slot_mapping, out, self.q, self.key_cache,
+            self.value_cache, self.cu_seqlens_q, self.seq_lens_k, self.block_tables,
+            max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k, scale=w.scale,
+            sinks=self.sinks, causal=w.causal,
+            partition_size=w.partition_size if partition_size is None else partition_size)
+        return out
+
 
 def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
     err = np.abs(got - ref)

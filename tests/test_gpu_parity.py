@@ -148,6 +148,60 @@ def test_block_size_144_as_nine_16_token_pages():
     assert torch.equal(base.view(torch.int16), out.view(torch.int16))
 
 
+FUSED = [
+    # (name, workload factory): decode only and mixed steps take the fused path
+    # (bf16, D = 128 / 256); fp32 and D = 64 take the scatter kernel first
+    ("decode-bf16-D128", lambda: wl.random_small(91, dtype=wl.BF16, num_seqs=6, head_dim=128,
+                                                  num_q_heads=8, num_kv_heads=2, max_prior=1400,
+                                                  max_q=1, with_sinks=True)),
+    ("mixed-bf16-D128", lambda: wl.random_small(92, dtype=wl.BF16, num_seqs=7, head_dim=128,
+                                                 num_q_heads=8, num_kv_heads=2, max_prior=900,
+                                                 max_q=40)),
+    ("mixed-bf16-D256", lambda: wl.random_small(93, dtype=wl.BF16, num_seqs=5, head_dim=256,
+                                                 num_q_heads=6, num_kv_heads=1, max_prior=700,
+                                                 max_q=20, block_size=32)),
+    ("decode-f32-D128", lambda: wl.random_small(94, dtype=wl.F32, num_seqs=4, head_dim=128,
+                                                 max_prior=500, max_q=1)),
+    ("mixed-bf16-D64", lambda: wl.random_small(95, dtype=wl.BF16, num_seqs=4, head_dim=64,
+                                                max_prior=300, max_q=9)),
+]
+
+
+@pytest.mark.parametrize("P", [0, -1, 32])
+@pytest.mark.parametrize("name,make", FUSED, ids=[f[0] for f in FUSED])
+def test_scatter_and_attend_equals_two_calls(name, make, P):
+    """pa_scatter_and_attend == pa_reshape_and_cache then pa_varlen_attention:
+    bit-identical caches and outputs (kwkr.cn kernel table: scatter, then attend)."""
+    w = make()
+    two = _run(w, partition_size=P)
+    one = DeviceWorkload(w)
+    one.fused_step(partition_size=P)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    assert torch.equal(dev_bits_t(two.key_cache), dev_bits_t(one.key_cache))
+    assert torch.equal(dev_bits_t(two.value_cache), dev_bits_t(one.value_cache))
+    assert torch.equal(dev_bits_t(two.out), dev_bits_t(one.out))
+
+
+@pytest.mark.parametrize("widx", [1, 3, 4])
+def test_scatter_and_attend_full_size(widx):
+    """The fused call on the full-size decode, mixed and long-decode workloads:
+    bit-identical to the two calls."""
+    w = wl.workload(widx)
+    two = _run(w)
+    one = DeviceWorkload(w)
+    one.fused_step()
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    assert torch.equal(dev_bits_t(two.key_cache), dev_bits_t(one.key_cache))
+    assert torch.equal(dev_bits_t(two.value_cache), dev_bits_t(one.value_cache))
+    assert torch.equal(dev_bits_t(two.out), dev_bits_t(one.out))
+
+
+def dev_bits_t(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
 def test_packing_independence():
     w = wl.random_small(83, dtype=wl.F32, num_seqs=4, max_prior=300, max_q=6)
     packed = from_dev(_run(w).out)
