@@ -20,7 +20,8 @@ scatter's reads and writes.  The accessed KV exceeds the 126 MB L2 on the decode
 workloads, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 1..4] [--no-cpu-baseline]
+                    [--workload 1..4] [--no-cpu-baseline] [--layout packed|padded]
+                    [--step two-call|fused]
 
 Under torchrun (N > 1) every rank runs its own independent batch (requests are
 independent units: weak scaling, no collective on the data path); timing is
@@ -338,12 +339,24 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(device)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     P_used = pa.pa_choose_partition_size(w.num_seqs, w.num_kv_heads, w.max_seqlen_k, P, sms)
-    launches_per_step = 1 + 1 + (1 if w.max_seqlen_q > 1 else 0) + (1 if P_used > 0 else 0)
+    tc_decode = w.dtype == "bf16" and w.head_dim in (128, 256)
+    # the fused call folds the scatter into the tensor-core decode kernel
+    fused = args.step == "fused"
+    scatter_launches = 0 if (fused and tc_decode) else 1
+    launches_per_step = (scatter_launches + 1 + (1 if w.max_seqlen_q > 1 else 0)
+                         + (1 if P_used > 0 else 0))
 
     def scatter(k_in=nk, v_in=nv, s_in=sm):
-        pa.pa_reshape_and_cache(k_in, v_in, kc, vc, s_in, stream=stream)
+        if not fused:
+            pa.pa_reshape_and_cache(k_in, v_in, kc, vc, s_in, stream=stream)
 
-    def attend(q_in=q, cu_in=cu, sl_in=sl, bt_in=bt, o=out):
+    def attend(q_in=q, cu_in=cu, sl_in=sl, bt_in=bt, o=out, k_in=nk, v_in=nv, s_in=sm):
+        if fused:
+            pa.pa_scatter_and_attend(k_in, v_in, s_in, o, q_in, kc, vc, cu_in, sl_in, bt_in,
+                                     max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k,
+                                     scale=w.scale, sinks=sk, causal=w.causal, partition_size=P,
+                                     workspace=ws, stream=stream)
+            return
         pa.pa_varlen_attention(o, q_in, kc, vc, cu_in, sl_in, bt_in,
                                max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k,
                                scale=w.scale, sinks=sk, causal=w.causal, partition_size=P,
@@ -403,7 +416,7 @@ def run_ours(args, rank, world, local):
                      (d_sl, h_sl), (d_bt, h_bt)):
             d.copy_(h, non_blocking=True)
         scatter(d_nk, d_nv, d_sm)
-        attend(d_q, d_cu, d_sl, d_bt)
+        attend(d_q, d_cu, d_sl, d_bt, k_in=d_nk, v_in=d_nv, s_in=d_sm)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -420,26 +433,33 @@ def run_ours(args, rank, world, local):
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device) / steps
     e2e_value, _ = metric_value(kind, work, e2e_s, world)
 
-    # ---------------- roofline of the dominant launch (the attention call)
+    # ---------------- roofline of the dominant launch (the attention call; with
+    # the fused step it also moves the scatter's bytes)
     hbm, bf16, peak_kind = measured_peaks()
-    t_bw = work["attention_bytes"] / (hbm * 1e9)
+    call_bytes = work["step_bytes"] if fused else work["attention_bytes"]
+    t_bw = call_bytes / (hbm * 1e9)
     t_fl = work["flops"] / (bf16 * 1e12)
     traffic = (NCU_TRAFFIC["bytes_per_launch"]
-               if NCU_TRAFFIC["sources_sha256"] == kernel_sources_hash() else None)
+               if NCU_TRAFFIC["sources_sha256"] == kernel_sources_hash() and not fused
+               else None)
     if kind == "decode" or (kind == "mixed" and t_bw >= t_fl):
-        roof = {"bound": "hbm", "achieved": round(work["attention_bytes"] / attn_avg_s / 1e9, 2),
+        roof = {"bound": "hbm", "achieved": round(call_bytes / attn_avg_s / 1e9, 2),
                 "peak": hbm, "unit": "GB/s"}
     else:
         roof = {"bound": "tensor", "achieved": round(work["flops"] / attn_avg_s / 1e12, 2),
                 "peak": bf16, "unit": "TFLOP/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = traffic
-    dec = ("paged_decode_tc_kernel" if w.dtype == "bf16" and w.head_dim in (128, 256)
-           else "paged_decode_kernel")
+    dec = "paged_decode_tc_kernel" if tc_decode else "paged_decode_kernel"
+    if fused and tc_decode:
+        dec += " (scatter fused)"
+    elif fused:
+        dec = "reshape_and_cache_kernel + " + dec
     roof["kernel"] = {"decode": f"{dec} + split_reduce_kernel",
                       "prefill": "paged_prefill_tc_kernel",
                       "mixed": f"{dec} + paged_prefill_tc_kernel + split_reduce_kernel"
-                      }[kind] + " (one attention call)"
+                      }[kind] + (" (one pa_scatter_and_attend call)" if fused
+                                 else " (one attention call)")
     roof["peak_source"] = (f"{peak_kind} (MEASURED_PEAKS.json "
                            f"{'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops'})"
                            if peak_kind == "measured" else "fallback")
@@ -459,7 +479,9 @@ def run_ours(args, rank, world, local):
                    "l2": "no flush: the KV read per step exceeds the 126 MB L2"
                          if work["kv"] > 2 * 126e6 else "no flush (KV partly L2-resident)",
                    "parallelism": f"independent batch per GPU x{world}",
-                   "layout": args.layout},
+                   "layout": args.layout,
+                   "step": ("pa_scatter_and_attend" if fused
+                            else "pa_reshape_and_cache + pa_varlen_attention")},
         "kv_gbs": round(world * work["step_bytes"] / step_s / 1e9, 2),
         "tflops": round(world * work["flops"] / step_s / 1e12, 3),
         "tokens_per_s": round(world * w_useful.total_q / step_s, 1),
@@ -489,6 +511,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layout", choices=["packed", "padded"], default="packed",
                     help="padded: the same batch padded to [B, T_max] (useful work counted)")
+    ap.add_argument("--step", choices=["fused", "two-call"], default="two-call",
+                    help="fused: one pa_scatter_and_attend call per step; two-call: "
+                         "pa_reshape_and_cache then pa_varlen_attention")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -168,7 +168,8 @@ int pa_choose_partition_size(int num_seqs, int num_kv_heads, int max_seqlen_k,
  *       pa_reshape_and_cache, with num_tokens == total_q: token t carries
  *       query row t's K and V (one step's packed tokens).  The slot of a
  *       single-query (decode) request's token must be the slot of its last
- *       key, position seq_lens_k - 1, as when a step appends that token.
+ *       key, position seq_lens_k - 1, as when a step appends that token,
+ *       and no token's slot may lie in a page that another request reads.
  *   every other argument: as for pa_varlen_attention (key_cache and
  *       value_cache are written).
  *

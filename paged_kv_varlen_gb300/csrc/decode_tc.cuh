@@ -579,24 +579,56 @@ __global__ void __launch_bounds__(224, 1)
         if (a.new_k != nullptr) {
             // Fused scatter of every row no decode item writes (rows of multi-query
             // requests, whose kernel runs after this one; rows whose slot lies
-            // past what the items read): one row per thread, all heads.
-            const int64_t rowv = (int64_t)hkv * D / 8;   // 16-byte pieces per row
-            for (int64_t t = (int64_t)blockIdx.x * 128 + tid; t < a.total_q;
-                 t += (int64_t)gridDim.x * 128) {
-                const int r = request_of_row(a.cu_seqlens_q, S, t);
-                const DtcReq q = dtc_request(a, r);
-                if (q.items > 0 && q.whole) continue;   // written by its item's producers
-                const int64_t slot = a.slot_mapping[t];
-                if (slot < 0 || slot >= a.num_slots) continue;
-                const uint4 *sk = reinterpret_cast<const uint4 *>(
-                    static_cast<const __nv_bfloat16 *>(a.new_k) + t * a.new_stride);
-                const uint4 *sv = reinterpret_cast<const uint4 *>(
-                    static_cast<const __nv_bfloat16 *>(a.new_v) + t * a.new_stride);
-                uint4 *dk = reinterpret_cast<uint4 *>(a.key_cache) + slot * rowv;
-                uint4 *dv = reinterpret_cast<uint4 *>(a.value_cache) + slot * rowv;
-                for (int64_t e = 0; e < rowv; ++e) {
-                    dk[e] = sk[e];
-                    dv[e] = sv[e];
+            // past what the items read).  Each softmax warp takes a contiguous
+            // range of rows, finds the first row's request once and walks the
+            // requests forward; a row's K and V pieces are spread over the lanes,
+            // all loads of a 128-piece chunk issued before its stores.
+            const int rowv = hkv * D / 8;   // 16-byte pieces per row
+            const int64_t nw = (int64_t)gridDim.x * 4;
+            const int64_t per = (a.total_q + nw - 1) / nw;
+            const int64_t t0 = ((int64_t)blockIdx.x * 4 + warp) * per;
+            const int64_t t1 = min(a.total_q, t0 + per);
+            if (t0 < t1) {
+                int r = request_of_row(a.cu_seqlens_q, S, t0);
+                int64_t c1 = a.cu_seqlens_q[r + 1];
+                DtcReq q = dtc_request(a, r);
+                for (int64_t t = t0; t < t1; ++t) {
+                    while (t >= c1 && r + 1 < S) {
+                        ++r;
+                        c1 = a.cu_seqlens_q[r + 1];
+                        q = dtc_request(a, r);
+                    }
+                    if (q.items > 0 && q.whole) {   // written by its item's producers
+                        t = c1 - 1;
+                        continue;
+                    }
+                    const int64_t slot = a.slot_mapping[t];
+                    if (slot < 0 || slot >= a.num_slots) continue;
+                    const uint4 *sk = reinterpret_cast<const uint4 *>(
+                        static_cast<const __nv_bfloat16 *>(a.new_k) + t * a.new_stride);
+                    const uint4 *sv = reinterpret_cast<const uint4 *>(
+                        static_cast<const __nv_bfloat16 *>(a.new_v) + t * a.new_stride);
+                    uint4 *dk = reinterpret_cast<uint4 *>(a.key_cache) + slot * rowv;
+                    uint4 *dv = reinterpret_cast<uint4 *>(a.value_cache) + slot * rowv;
+                    for (int e0 = 0; e0 < rowv; e0 += 128) {
+                        uint4 kx[4], vx[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int e = e0 + u * 32 + lane;
+                            if (e < rowv) {
+                                kx[u] = __ldg(sk + e);
+                                vx[u] = __ldg(sv + e);
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int e = e0 + u * 32 + lane;
+                            if (e < rowv) {
+                                dk[e] = kx[u];
+                                dv[e] = vx[u];
+                            }
+                        }
+                    }
                 }
             }
         }
