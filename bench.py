@@ -1,10 +1,10 @@
 """Benchmark of the paged varlen attention hot path on GB300.
 
 One step = one pass of the whole hot path over one batch: the KV scatter of
-this step's tokens (pa_reshape_and_cache), then attention over the packed
-query rows and paged K/V (pa_varlen_attention: the split-KV decode kernel and
-its shared reduce for single-query rows, the tcgen05 kernel for multi-query
-rows).
+this step's tokens, then attention over the packed query rows and paged K/V
+(the split-KV decode kernel and its shared reduce for single-query rows, the
+tcgen05 kernel for multi-query rows) -- one pa_scatter_and_attend call
+(``--step two-call``: pa_reshape_and_cache then pa_varlen_attention).
 
 Default workload (the one the headline metric is quoted on): the GQA decode
 batch -- 32 requests with contexts U[512, 8192], (H_q, H_kv, D) = (32, 8, 128),
@@ -53,7 +53,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per attention call from an ncu
 # capture, valid only for the kernel sources whose hash is recorded beside it.
-NCU_TRAFFIC = {"sources_sha256": None, "bytes_per_launch": None}
+# DRAM bytes (read + write) of one paged_decode_tc_kernel launch on workload 1,
+# from ncu (dram__bytes_read.sum + dram__bytes_write.sum); valid while the
+# kernel sources hash to the value below.
+NCU_TRAFFIC = {"sources_sha256": "c1612917ff17e6f8bd1817656164f235fa823dfd38613e38805e8e363c602961",
+               "bytes_per_launch": 526311424 + 5195008, "workload": 1}
 
 
 def kernel_sources_hash() -> str:
@@ -340,11 +344,9 @@ def run_ours(args, rank, world, local):
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     P_used = pa.pa_choose_partition_size(w.num_seqs, w.num_kv_heads, w.max_seqlen_k, P, sms)
     tc_decode = w.dtype == "bf16" and w.head_dim in (128, 256)
-    # the fused call folds the scatter into the tensor-core decode kernel
+    # fused: one pa_scatter_and_attend call (the decode kernel overlaps the scatter)
     fused = args.step == "fused"
-    scatter_launches = 0 if (fused and tc_decode) else 1
-    launches_per_step = (scatter_launches + 1 + (1 if w.max_seqlen_q > 1 else 0)
-                         + (1 if P_used > 0 else 0))
+    launches_per_step = 1 + 1 + (1 if w.max_seqlen_q > 1 else 0) + (1 if P_used > 0 else 0)
 
     def scatter(k_in=nk, v_in=nv, s_in=sm):
         if not fused:
@@ -440,8 +442,8 @@ def run_ours(args, rank, world, local):
     t_bw = call_bytes / (hbm * 1e9)
     t_fl = work["flops"] / (bf16 * 1e12)
     traffic = (NCU_TRAFFIC["bytes_per_launch"]
-               if NCU_TRAFFIC["sources_sha256"] == kernel_sources_hash() and not fused
-               else None)
+               if NCU_TRAFFIC["sources_sha256"] == kernel_sources_hash()
+               and NCU_TRAFFIC.get("workload") == args.workload else None)
     if kind == "decode" or (kind == "mixed" and t_bw >= t_fl):
         roof = {"bound": "hbm", "achieved": round(call_bytes / attn_avg_s / 1e9, 2),
                 "peak": hbm, "unit": "GB/s"}
@@ -451,10 +453,8 @@ def run_ours(args, rank, world, local):
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = traffic
     dec = "paged_decode_tc_kernel" if tc_decode else "paged_decode_kernel"
-    if fused and tc_decode:
-        dec += " (scatter fused)"
-    elif fused:
-        dec = "reshape_and_cache_kernel + " + dec
+    if fused:
+        dec = "scatter_rows_kernel + " + dec
     roof["kernel"] = {"decode": f"{dec} + split_reduce_kernel",
                       "prefill": "paged_prefill_tc_kernel",
                       "mixed": f"{dec} + paged_prefill_tc_kernel + split_reduce_kernel"
@@ -511,7 +511,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layout", choices=["packed", "padded"], default="packed",
                     help="padded: the same batch padded to [B, T_max] (useful work counted)")
-    ap.add_argument("--step", choices=["fused", "two-call"], default="two-call",
+    ap.add_argument("--step", choices=["fused", "two-call"], default="fused",
                     help="fused: one pa_scatter_and_attend call per step; two-call: "
                          "pa_reshape_and_cache then pa_varlen_attention")
     args = ap.parse_args(argv)

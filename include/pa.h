@@ -7,8 +7,8 @@
  *   pa_varlen_attention    attention for packed query rows over paged K/V
  *   pa_split_kv_reduce     merge split-KV partial results
  *
- * and pa_scatter_and_attend runs the first two as one call (the scatter fused
- * into the decode kernel).
+ * and pa_scatter_and_attend runs the first two as one call (the decode kernel
+ * overlapping the scatter).
  *
  * Sources: "vllm-metal ... Paged Attention kernels" (kwkr.cn) -- section
  * "What is Paged Attention" (pages + block tables), the kernel table
@@ -161,24 +161,18 @@ int pa_choose_partition_size(int num_seqs, int num_kv_heads, int max_seqlen_k,
 /*
  * pa_scatter_and_attend -- one model step in one call: pa_reshape_and_cache of
  * this step's K/V rows, then pa_varlen_attention.  (kwkr.cn kernel table: the
- * scatter runs before the attention kernel that reads the new rows; here the
- * two are fused.)
+ * scatter runs before the attention kernel that reads the new rows.)
  *
  *   key, value, kv_token_stride, slot_mapping, num_tokens: as for
- *       pa_reshape_and_cache, with num_tokens == total_q: token t carries
- *       query row t's K and V (one step's packed tokens).  The slot of a
- *       single-query (decode) request's token must be the slot of its last
- *       key, position seq_lens_k - 1, as when a step appends that token,
- *       and no token's slot may lie in a page that another request reads.
+ *       pa_reshape_and_cache, with num_tokens == total_q (token t carries
+ *       query row t's K and V: one step's packed tokens).
  *   every other argument: as for pa_varlen_attention (key_cache and
  *       value_cache are written).
  *
- * With bf16 caches at head_dim 128 or 256 and 16-byte-aligned K/V rows the
- * scatter runs inside the decode kernel: the CTA that reads a decode
- * request's last tile writes that request's row first, and the rows of
- * multi-query requests are written before their kernel starts -- a step of
- * decode rows is a single launch (plus the reduce when it splits).  Otherwise
- * the scatter kernel runs first.  Result: the two calls in order.
+ * Result: exactly the two calls in order.  The kernels overlap: with bf16
+ * caches at head_dim 128 or 256 the decode kernel is launched while the
+ * scatter runs (programmatic dependent launch) and sets up its work plan,
+ * page ids and pipeline meanwhile; only its K/V loads wait for the scatter.
  * Errors: those of both calls; PA_ERR_INVALID_ARG if num_tokens != total_q.
  */
 pa_status pa_scatter_and_attend(const void *key, const void *value, int64_t kv_token_stride,

@@ -34,11 +34,12 @@
 //    the end of an item sum the exp-sums and write the output or the partial.
 //    Value rows past the last key of a partial tile are zeroed before the PV
 //    MMA reads them (a zero weight times a NaN pool slot would still be NaN).
-//  * Fused scatter (pa_scatter_and_attend): the producer that loads a decode
-//    request's last tile first writes that request's newest K (V) row for its
-//    KV head into the cache and fences it for TMA; the softmax warps scatter,
-//    while the pipeline fills, every row no decode item reads (rows of the
-//    multi-query requests, whose kernel runs after this one).
+//  * Programmatic dependent launch: the kernel may start while the previous
+//    kernel of the stream runs.  It waits for that kernel before its first
+//    global read -- or, after this step's scatter (which writes only the new
+//    K/V rows), only before the K/V loads, so its setup, work plan and first
+//    page ids overlap the scatter -- and lets the next kernel (the reduce)
+//    be scheduled from its start.
 //  * Every barrier wait is bounded (pa::mbar_wait); nothing spins forever.
 #pragma once
 
@@ -89,20 +90,17 @@ struct DtcReq {
     int N;       // keys
     int wfull;   // work of an item of a full partition
     int wlast;   // work of an item of the last partition
-    int whole;   // the items reach the request's last key (its newest token)
 };
 
 // c0, c1 = cu_seqlens_q[r], cu_seqlens_q[r + 1]; sl = seq_lens_k[r]
 __device__ __forceinline__ DtcReq dtc_request_from(const DecodeTcArgs &a, int c0, int c1, int sl) {
-    DtcReq q = {0, 0, 0, 0, 0, 0};
+    DtcReq q = {0, 0, 0, 0, 0};
     if (c1 - c0 != 1) return q;                       // multi-query request: other kernel
     int N = max(0, min(sl, a.max_blocks_per_seq * a.block_size));
     q.N = N;
-    q.whole = N >= 1 && min(sl, a.max_blocks_per_seq * a.block_size) == sl;
     const int P = a.partition_size;
     if (P > 0) {
         // partials exist for max_parts partitions only (the reduce reads no more)
-        if (N > a.max_parts * P) q.whole = 0;
         N = min(N, a.max_parts * P);
         q.N = N;
         q.np = (N + P - 1) / P;
@@ -260,6 +258,7 @@ __global__ void __launch_bounds__(224, 1)
     const int hkv = a.num_kv_heads;
 
     // ---------------------------------------------------------------- setup
+    pdl_trigger();   // the reduce (or the next kernel) may be scheduled meanwhile
     if (tid == 0) {
         for (int s = 0; s < C::NR; ++s) {
             mbar_init(bar_k_full + 8 * s, 1);   // expect-tx arrival, TMA bytes
@@ -294,6 +293,11 @@ __global__ void __launch_bounds__(224, 1)
         *reinterpret_cast<uint4 *>(smem + C::OFF_Q + 16 * i) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
 
+    // the launch may overlap the previous kernel of the stream: wait for it
+    // before reading global memory (only before the K/V loads when that
+    // kernel is this step's scatter)
+    if (!a.after_scatter) pdl_wait();
+
     // ---- this CTA's items: those whose cumulative work starts in [lo, hi)
     {
         int64_t acc = 0;
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(224, 1)
         int64_t carry = 0;
         for (int base = 0; base < S && lo < hi; base += C::THREADS) {
             const int r = base + tid;
-            const DtcReq q = r < S ? dtc_request(a, r) : DtcReq{0, 0, 0, 0, 0, 0};
+            const DtcReq q = r < S ? dtc_request(a, r) : DtcReq{0, 0, 0, 0, 0};
             const int64_t w = dtc_work(q, hkv);
             int64_t tot;
             const int64_t E = carry + dtc_block_scan<C::THREADS>(w, scratch, &tot) - w;
@@ -394,6 +398,7 @@ __global__ void __launch_bounds__(224, 1)
             fetch_pages(la, jl, t);
             if (valid(la)) adv(la, jl, itl);
         }
+        if (a.after_scatter) pdl_wait();   // this step's K/V rows are in the caches
         int t = 0, issued = 0;
         int q_last[2] = {-1, -1};
         while (valid(cur)) {
@@ -401,22 +406,6 @@ __global__ void __launch_bounds__(224, 1)
             if (valid(la)) adv(la, jl, itl);
             cp_async_wait<C::PGR - 1>();   // tile t's page ids have landed
             __syncwarp();
-            if (a.new_k != nullptr && cur.q.whole && cur.k1 == cur.q.N && j == cur.ntiles - 1) {
-                // fused scatter: this step's row of the request is its last key,
-                // which this tile reads; write it first (K here, V in warp 5)
-                const int64_t slot = a.slot_mapping[cur.row];
-                if (slot >= 0 && slot < a.num_slots) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        static_cast<const __nv_bfloat16 *>(is_k ? a.new_k : a.new_v) +
-                        cur.row * a.new_stride + (int64_t)cur.h * D);
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        static_cast<__nv_bfloat16 *>(is_k ? a.key_cache : a.value_cache) +
-                        (slot * hkv + cur.h) * D);
-                    for (int e = lane; e < D / 8; e += 32) dst[e] = src[e];
-                    fence_proxy_async_global();   // before this warp's TMA reads it
-                }
-                __syncwarp();
-            }
             int bad = 0;
             if (lane == 0) {
                 if (is_k && j == 0) {   // Q^T of the item, rows = its G heads
@@ -576,62 +565,6 @@ __global__ void __launch_bounds__(224, 1)
         const float qsc = a.qscale;
         const int Hq = a.num_q_heads;
         const bool split = a.partition_size > 0;
-        if (a.new_k != nullptr) {
-            // Fused scatter of every row no decode item writes (rows of multi-query
-            // requests, whose kernel runs after this one; rows whose slot lies
-            // past what the items read).  Each softmax warp takes a contiguous
-            // range of rows, finds the first row's request once and walks the
-            // requests forward; a row's K and V pieces are spread over the lanes,
-            // all loads of a 128-piece chunk issued before its stores.
-            const int rowv = hkv * D / 8;   // 16-byte pieces per row
-            const int64_t nw = (int64_t)gridDim.x * 4;
-            const int64_t per = (a.total_q + nw - 1) / nw;
-            const int64_t t0 = ((int64_t)blockIdx.x * 4 + warp) * per;
-            const int64_t t1 = min(a.total_q, t0 + per);
-            if (t0 < t1) {
-                int r = request_of_row(a.cu_seqlens_q, S, t0);
-                int64_t c1 = a.cu_seqlens_q[r + 1];
-                DtcReq q = dtc_request(a, r);
-                for (int64_t t = t0; t < t1; ++t) {
-                    while (t >= c1 && r + 1 < S) {
-                        ++r;
-                        c1 = a.cu_seqlens_q[r + 1];
-                        q = dtc_request(a, r);
-                    }
-                    if (q.items > 0 && q.whole) {   // written by its item's producers
-                        t = c1 - 1;
-                        continue;
-                    }
-                    const int64_t slot = a.slot_mapping[t];
-                    if (slot < 0 || slot >= a.num_slots) continue;
-                    const uint4 *sk = reinterpret_cast<const uint4 *>(
-                        static_cast<const __nv_bfloat16 *>(a.new_k) + t * a.new_stride);
-                    const uint4 *sv = reinterpret_cast<const uint4 *>(
-                        static_cast<const __nv_bfloat16 *>(a.new_v) + t * a.new_stride);
-                    uint4 *dk = reinterpret_cast<uint4 *>(a.key_cache) + slot * rowv;
-                    uint4 *dv = reinterpret_cast<uint4 *>(a.value_cache) + slot * rowv;
-                    for (int e0 = 0; e0 < rowv; e0 += 128) {
-                        uint4 kx[4], vx[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int e = e0 + u * 32 + lane;
-                            if (e < rowv) {
-                                kx[u] = __ldg(sk + e);
-                                vx[u] = __ldg(sv + e);
-                            }
-                        }
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int e = e0 + u * 32 + lane;
-                            if (e < rowv) {
-                                dk[e] = kx[u];
-                                dv[e] = vx[u];
-                            }
-                        }
-                    }
-                }
-            }
-        }
         DtcIter cur = it0;
         int gt = 0, itn = 0, ie = 0;
         while (valid(cur)) {
@@ -846,8 +779,8 @@ cudaError_t launch_decode_tc_t(const CUtensorMap &qmap, const CUtensorMap &kmap,
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qmap, kmap, vmap, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, qmap, kmap, vmap,
+                      a);
 }
 
 template <int D>

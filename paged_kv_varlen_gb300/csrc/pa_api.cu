@@ -346,14 +346,12 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         }
     };
 
-    // 0) this step's K/V rows (pa_scatter_and_attend): fused into the tensor-core
-    //    decode kernel when it runs and the rows are 16-byte aligned, else the
-    //    scatter kernel first
+    // 0) this step's K/V rows (pa_scatter_and_attend): the scatter kernel; the
+    //    tensor-core decode kernel launched next overlaps it (programmatic
+    //    dependent launch) and only its K/V loads wait for it
     const bool tc_decode = dtype == PA_BF16 && (head_dim == 128 || head_dim == 256);
-    const bool fuse = fs && tc_decode && aligned16(fs->key) && aligned16(fs->value) &&
-                      (fs->stride * 2) % 16 == 0;
     cudaError_t ce;
-    if (fs && !fuse) {
+    if (fs) {
         const int64_t eb = dtype == PA_F32 ? 4 : 2;
         ce = launch_reshape_and_cache(fs->key, fs->value, fs->stride * eb, const_cast<void *>(key_cache),
                                       const_cast<void *>(value_cache), fs->slot_mapping, total_q,
@@ -396,20 +394,9 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         da.part_l = part_l;
         da.box_rows = dbox;
         da.err = dev.err;
-        da.new_k = fuse ? fs->key : nullptr;
-        da.new_v = fuse ? fs->value : nullptr;
-        da.new_stride = fuse ? fs->stride : 0;
-        da.slot_mapping = fuse ? fs->slot_mapping : nullptr;
-        da.key_cache = const_cast<void *>(key_cache);
-        da.value_cache = const_cast<void *>(value_cache);
-        da.num_slots = num_blocks * block_size;
-        da.total_q = total_q;
+        da.after_scatter = fs != nullptr ? 1 : 0;
         const int64_t items_max = (int64_t)num_seqs * num_kv_heads * max_parts;
-        // (a fused scatter needs the kernel even with no decode rows)
-        const int grid = (int)std::max<int64_t>(
-            1, std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148,
-                                 fuse ? std::max<int64_t>(items_max, (total_q + 127) / 128)
-                                      : items_max));
+        const int grid = (int)std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, items_max);
         ce = head_dim == 128 ? launch_decode_tc_d128(group, qmap_d, kmap_d, vmap_d, da, grid, s)
                              : launch_decode_tc_d256(group, qmap_d, kmap_d, vmap_d, da, grid, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode_tc launch");
@@ -488,6 +475,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         ra.partition_size = P;
         ra.num_q_heads = num_q_heads;
         ra.sinks = sinks;
+        ra.meta_before_wait = 1;   // the kernels before it write only out / partials
         ce = launch_reduce(e, head_dim, ra, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "split_reduce launch");
     }
@@ -565,6 +553,7 @@ PA_API pa_status pa_split_kv_reduce(void *out, const float *part_out, const floa
     ra.partition_size = partition_size;
     ra.num_q_heads = num_q_heads;
     ra.sinks = sinks;
+    ra.meta_before_wait = 0;   // the previous kernel may have written anything
     cudaError_t ce = launch_reduce(dtype == PA_F32 ? 4 : 2, head_dim, ra,
                                    static_cast<cudaStream_t>(stream));
     if (ce != cudaSuccess) return cuda_fail(ce, "split_reduce launch");

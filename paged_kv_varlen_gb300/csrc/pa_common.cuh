@@ -90,10 +90,15 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, long l
         if (clock64() - t0 > limit) return;
 }
 
-// Generic-proxy writes to global memory made visible to later async-proxy
-// (TMA) reads of the same addresses.
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream runs;
+// pdl_wait() blocks the calling thread until that kernel has completed and
+// its memory writes are visible (at once when there is none, or when it was
+// launched without the attribute).  pdl_trigger() lets the next kernel start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- cp.async

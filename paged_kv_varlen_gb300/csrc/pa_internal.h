@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pa {
 
 constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
@@ -76,16 +78,10 @@ struct DecodeTcArgs {
     float *part_l;             // [num_seqs, max_parts, Hq]
     int box_rows;              // rows per K/V TMA box: divides 128, the block and partition sizes
     int *err;                  // device error word
-    // Fused scatter (pa_scatter_and_attend; new_k == nullptr: none): this
-    // step's K/V row of every query row t goes to slot slot_mapping[t].
-    const void *new_k;         // [total_q, Hkv, D] bf16 rows, new_stride elements apart
-    const void *new_v;
-    int64_t new_stride;
-    const int64_t *slot_mapping;
-    void *key_cache;           // [num_slots, Hkv, D] bf16 (the caches the kernel reads)
-    void *value_cache;
-    int64_t num_slots;         // num_blocks * block_size
-    int64_t total_q;
+    // 1: the previous kernel of the stream is the scatter of this step's K/V
+    // rows (it writes nothing else the kernel reads): only the K/V loads wait
+    // for it.  0: the whole kernel waits for the previous kernel first.
+    int after_scatter;
 };
 
 // Keys per K/V tile of the tensor-core kernel and query rows per block.
@@ -106,7 +102,27 @@ struct ReduceArgs {
     int partition_size;
     int num_q_heads;
     const float *sinks;
+    int meta_before_wait;      // 1: cu_seqlens_q / seq_lens_k / sinks are read before
+                               // waiting on the previous kernel (it does not write them)
 };
+
+// Launches `kern` with programmatic stream serialization: it may start while
+// the previous kernel of the stream runs and waits for it with pdl_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Per (dtype, head_dim) launchers; `group` = Hq / Hkv in 1..8.
 // Each returns the launch error (cudaSuccess if launched).

@@ -21,12 +21,14 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
     const int r = blockIdx.x;
     const int hq = blockIdx.y;
     const int Hq = a.num_q_heads;
+    if (!a.meta_before_wait) pdl_wait();   // (launched early: see launch_reduce_t)
     const int c0 = a.cu_seqlens_q[r];
     if (a.cu_seqlens_q[r + 1] - c0 != 1) return;
     const int N = max(0, a.seq_lens_k[r]);
     const int nparts = min((N + a.partition_size - 1) / a.partition_size, a.max_parts);
     const int tid = threadIdx.x;
     const float sk2 = a.sinks ? a.sinks[hq] * kLog2e : -INFINITY;
+    if (a.meta_before_wait) pdl_wait();    // the partials come from the previous kernel
 
     // M = max over partitions of m_p, and over the sink logit
     float mx = -INFINITY;
@@ -91,9 +93,10 @@ static cudaError_t launch_reduce_t(const ReduceArgs &a, cudaStream_t stream) {
                                              (int)smem);
         if (e != cudaSuccess) return e;
     }
-    dim3 grid(a.num_seqs, a.num_q_heads);
-    kern<<<grid, kReduceThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    // launched while the kernel writing the partials still runs; each CTA
+    // waits for it (pdl_wait) before reading them
+    return launch_pdl(kern, dim3(a.num_seqs, a.num_q_heads), dim3(kReduceThreads), smem, stream,
+                      a);
 }
 
 cudaError_t launch_reduce(int elem_bytes, int head_dim, const ReduceArgs &a, cudaStream_t stream) {

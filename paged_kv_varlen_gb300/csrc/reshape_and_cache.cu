@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
                         int64_t stride_bytes, uint8_t *__restrict__ kc, uint8_t *__restrict__ vc,
                         const int64_t *__restrict__ slots, int64_t num_tokens, int64_t row_bytes,
                         int64_t num_slots) {
+    pdl_trigger();   // the attention kernel may start its setup meanwhile
     const int64_t t = (int64_t)blockIdx.x * kScatterWarps + (threadIdx.x >> 5);
     if (t >= num_tokens) return;
     const int lane = threadIdx.x & 31;

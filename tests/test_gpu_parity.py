@@ -9,6 +9,7 @@ import math
 import zlib
 
 import numpy as np
+
 import pytest
 import torch
 
@@ -164,6 +165,11 @@ FUSED = [
                                                  max_prior=500, max_q=1)),
     ("mixed-bf16-D64", lambda: wl.random_small(95, dtype=wl.BF16, num_seqs=4, head_dim=64,
                                                 max_prior=300, max_q=9)),
+    # 600 short decode requests: CTAs whose work spans several 224-request
+    # chunks of the decode kernel's plan scan
+    ("decode-600-short", lambda: wl.random_small(96, dtype=wl.BF16, num_seqs=600, head_dim=128,
+                                                  num_q_heads=4, num_kv_heads=1, max_prior=200,
+                                                  max_q=1)),
 ]
 
 
@@ -171,7 +177,8 @@ FUSED = [
 @pytest.mark.parametrize("name,make", FUSED, ids=[f[0] for f in FUSED])
 def test_scatter_and_attend_equals_two_calls(name, make, P):
     """pa_scatter_and_attend == pa_reshape_and_cache then pa_varlen_attention:
-    bit-identical caches and outputs (kwkr.cn kernel table: scatter, then attend)."""
+    bit-identical caches and outputs (kwkr.cn kernel table: scatter, then attend;
+    the overlapped decode launch must not read a K/V row before it is written)."""
     w = make()
     two = _run(w, partition_size=P)
     one = DeviceWorkload(w)
