@@ -126,7 +126,8 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t kv_to
  *
  * Supported: dtype F32 or BF16; head_dim 64, 128 or 256; H_q a multiple of
  * H_kv with H_q / H_kv <= 8; block_size a multiple of 8 (<= 1024); num_seqs
- * <= 65535.  Single-query rows (decode) run on a bandwidth kernel with
+ * <= 65535; with split-KV, at most 12288 partitions per request
+ * (ceil(max_seqlen_k / partition_size)).  Single-query rows (decode) run on a bandwidth kernel with
  * split-KV; multi-query rows (speculative verify, prefill) run on the
  * multi-row kernel.
  * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE,
@@ -206,7 +207,8 @@ pa_status pa_scatter_and_attend(const void *key, const void *value, int64_t kv_t
  *   part_sum  device float32 [num_seqs, max_parts, H_q]: l_p = sum of
  *             2^(t_j - m_p) over the partition
  *   out       device [total_q, H_q, D] in `dtype`
- * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED (head_dim), PA_ERR_CUDA.
+ * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED (head_dim, or max_parts >
+ * 12288: the weights live in shared memory), PA_ERR_CUDA.
  */
 pa_status pa_split_kv_reduce(void *out, const float *part_out, const float *part_max,
                              const float *part_sum, const int32_t *cu_seqlens_q,

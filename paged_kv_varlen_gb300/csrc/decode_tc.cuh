@@ -10,8 +10,10 @@
 //
 // GB300 design (persistent: one CTA per SM, 224 threads)
 //  * A work item is (request, KV head, partition).  Every CTA scans the batch
-//    once, weighs each item by its key tiles plus one, and takes, in order,
-//    the items whose cumulative work starts inside its 1/gridDim share.
+//    once, weighs each item by five per key tile plus three (an item's fixed
+//    cost -- Q load, pipeline turn, epilogue -- measured at about 0.6 tile), and
+//    takes, in order, the items whose cumulative work starts inside its
+//    1/gridDim share.
 //  * Keys are the MMA rows: S^T[128 keys x 16] = K_tile . Q^T with the G query
 //    heads of the KV head padded to N = 16, so one M = 128 MMA per 16-dim step
 //    serves the whole GQA group however small G is; O^T[d x 16] += V^T . P^T
@@ -83,7 +85,7 @@ struct DtcCfg {
 };
 
 // Work of one decode request: its (partition, KV head) items, ordered
-// partition-major, each weighed by its tiles plus one.
+// partition-major, each weighed by five per key tile plus three.
 struct DtcReq {
     int items;   // 0 when the request has no decode work here
     int np;      // partitions
@@ -105,11 +107,11 @@ __device__ __forceinline__ DtcReq dtc_request_from(const DecodeTcArgs &a, int c0
         q.N = N;
         q.np = (N + P - 1) / P;
         if (q.np == 0) return q;                      // no keys: the reduce writes zeros
-        q.wfull = (P + 127) / 128 + 1;
-        q.wlast = (N - (q.np - 1) * P + 127) / 128 + 1;
+        q.wfull = 5 * ((P + 127) / 128) + 3;
+        q.wlast = 5 * ((N - (q.np - 1) * P + 127) / 128) + 3;
     } else {
         q.np = 1;                                     // one item, even with no keys
-        q.wfull = q.wlast = (N + 127) / 128 + 1;
+        q.wfull = q.wlast = 5 * ((N + 127) / 128) + 3;
     }
     q.items = q.np * a.num_kv_heads;
     return q;

@@ -285,6 +285,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
                                            dev.sm_count);
     const int max_parts = (P > 0 && max_seqlen_k > 0) ? ceil_div(max_seqlen_k, P) : 1;
     float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
+    if (P > 0 && max_parts > kMaxReduceParts) return PA_ERR_UNSUPPORTED;
     if (P > 0) {
         const SplitLayout L = split_layout(num_seqs, max_parts, num_q_heads, head_dim);
         if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
@@ -537,7 +538,7 @@ PA_API pa_status pa_split_kv_reduce(void *out, const float *part_out, const floa
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     if (num_seqs > 0x7fffffff || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
-    if (max_parts > 12288) return PA_ERR_UNSUPPORTED;   // weights live in shared memory
+    if (max_parts > kMaxReduceParts) return PA_ERR_UNSUPPORTED;
     if (!out || !part_out || !part_max || !part_sum || !cu_seqlens_q || !seq_lens_k)
         return PA_ERR_INVALID_ARG;
     if (!aligned16(part_out) || (reinterpret_cast<uintptr_t>(out) & 3)) return PA_ERR_INVALID_ARG;

@@ -177,6 +177,9 @@ PA_DECLARE_DTC(launch_decode_tc_d256)
 #undef PA_DECLARE_DTC
 
 cudaError_t launch_reduce(int elem_bytes, int head_dim, const ReduceArgs &a, cudaStream_t stream);
+// Partitions per request the reduce takes (its weights and maxima live in
+// shared memory: 8 bytes per partition).
+constexpr int kMaxReduceParts = 12288;
 
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t stride_bytes,
                                      void *key_cache, void *value_cache, const int64_t *slots,

@@ -2,10 +2,12 @@
 // log2-space (max, exp-sum) pair plus a normalised partial output; one shared
 // reduce kernel merges them, and the GQA decode path reuses it).
 //
-// One CTA per (request, query head).  The partition weights
-// w_p = l_p * 2^(m_p - M) are computed once into shared memory, then each
-// thread combines a 16-byte slice of the head dimension across partitions
-// (coalesced reads of the [num_seqs, max_parts, Hq, D] partial outputs).
+// One CTA per (request, query head).  The partition maxima and exp-sums are
+// read in one pass and the weights w_p = l_p * 2^(m_p - M) kept in shared
+// memory; then thread (g, c) combines the 16-byte slice c of the head
+// dimension over every PG-th partition starting at g, four loads in flight
+// (coalesced reads of the [num_seqs, max_parts, Hq, D] partial outputs), and
+// the PG partial sums are added through shared memory.
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -15,9 +17,12 @@ constexpr int kReduceThreads = 128;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const ReduceArgs a) {
-    extern __shared__ float wsh[];   // [max_parts] weights
+    extern __shared__ float wsh[];   // [2][max_parts]: partition weights, then maxima
+    constexpr int LANES = D / 4;                 // float4 slices of one head's row
+    constexpr int PG = kReduceThreads / LANES;   // partition groups working in parallel
     __shared__ float red[kReduceThreads / 32];
     __shared__ float Msh, densh;
+    __shared__ float4 part[PG > 1 ? PG - 1 : 1][LANES];
     const int r = blockIdx.x;
     const int hq = blockIdx.y;
     const int Hq = a.num_q_heads;
@@ -29,11 +34,18 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
     const int tid = threadIdx.x;
     const float sk2 = a.sinks ? a.sinks[hq] * kLog2e : -INFINITY;
     if (a.meta_before_wait) pdl_wait();    // the partials come from the previous kernel
+    float *msh = wsh + a.max_parts;
 
-    // M = max over partitions of m_p, and over the sink logit
+    // M = max over partitions of m_p, and over the sink logit (m_p and l_p are
+    // read together, one pass)
     float mx = -INFINITY;
-    for (int p = tid; p < nparts; p += kReduceThreads)
-        mx = fmaxf(mx, a.part_m[((int64_t)r * a.max_parts + p) * Hq + hq]);
+    for (int p = tid; p < nparts; p += kReduceThreads) {
+        const int64_t slot = ((int64_t)r * a.max_parts + p) * Hq + hq;
+        const float m = a.part_m[slot];
+        wsh[p] = a.part_l[slot];
+        msh[p] = m;
+        mx = fmaxf(mx, m);
+    }
     mx = warp_max(mx);
     if ((tid & 31) == 0) red[tid >> 5] = mx;
     __syncthreads();
@@ -46,13 +58,12 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
     const float M = Msh;
     float sum = 0.f;
     for (int p = tid; p < nparts; p += kReduceThreads) {
-        const int64_t slot = ((int64_t)r * a.max_parts + p) * Hq + hq;
-        const float w = a.part_l[slot] * exp2f(a.part_m[slot] - M);
+        const float w = wsh[p] * exp2f(msh[p] - M);
         wsh[p] = w;
         sum += w;
     }
     sum = warp_sum(sum);
-    __syncthreads();   // red[] reuse
+    __syncthreads();   // red[] reuse; wsh complete
     if ((tid & 31) == 0) red[tid >> 5] = sum;
     __syncthreads();
     if (tid == 0) {
@@ -64,29 +75,61 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
     __syncthreads();
     const float den = densh;
 
-    constexpr int VEC = 4;
-    constexpr int LANES = D / VEC;
-    T *out = reinterpret_cast<T *>(a.out) + ((int64_t)c0 * Hq + hq) * D;
-    for (int c = tid; c < LANES; c += kReduceThreads) {
-        float acc[VEC] = {0.f, 0.f, 0.f, 0.f};
-        for (int p = 0; p < nparts; ++p) {
-            const float w = wsh[p];
-            const float4 o = *reinterpret_cast<const float4 *>(
-                a.part_o + (((int64_t)r * a.max_parts + p) * Hq + hq) * D + c * VEC);
-            acc[0] = fmaf(w, o.x, acc[0]);
-            acc[1] = fmaf(w, o.y, acc[1]);
-            acc[2] = fmaf(w, o.z, acc[2]);
-            acc[3] = fmaf(w, o.w, acc[3]);
-        }
+    // O = sum_p w_p o_p / den: thread (g, c) sums the float4 slice c over the
+    // partitions p = g, g + PG, ... (loads issued four at a time), then the PG
+    // groups are added through shared memory
+    const int c = tid % LANES, g = tid / LANES;
+    const float *po = a.part_o + ((int64_t)r * a.max_parts * Hq + hq) * D + c * 4;
+    const int64_t pstride = (int64_t)Hq * D;   // floats between partitions
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int p = g;
+    for (; p + 3 * PG < nparts; p += 4 * PG) {
+        float4 o[4];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-            out[c * VEC + e] = Elem<T>::to_store(nparts > 0 ? acc[e] / den : 0.f);
+        for (int u = 0; u < 4; ++u)
+            o[u] = *reinterpret_cast<const float4 *>(po + (int64_t)(p + u * PG) * pstride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float w = wsh[p + u * PG];
+            acc[0] = fmaf(w, o[u].x, acc[0]);
+            acc[1] = fmaf(w, o[u].y, acc[1]);
+            acc[2] = fmaf(w, o[u].z, acc[2]);
+            acc[3] = fmaf(w, o[u].w, acc[3]);
+        }
+    }
+    for (; p < nparts; p += PG) {
+        const float4 o = *reinterpret_cast<const float4 *>(po + (int64_t)p * pstride);
+        const float w = wsh[p];
+        acc[0] = fmaf(w, o.x, acc[0]);
+        acc[1] = fmaf(w, o.y, acc[1]);
+        acc[2] = fmaf(w, o.z, acc[2]);
+        acc[3] = fmaf(w, o.w, acc[3]);
+    }
+    if (PG > 1) {
+        if (g > 0) part[g - 1][c] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncthreads();
+        if (g == 0) {
+#pragma unroll
+            for (int k = 0; k < PG - 1; ++k) {
+                const float4 o = part[k][c];
+                acc[0] += o.x;
+                acc[1] += o.y;
+                acc[2] += o.z;
+                acc[3] += o.w;
+            }
+        }
+    }
+    if (g == 0) {
+        T *out = reinterpret_cast<T *>(a.out) + ((int64_t)c0 * Hq + hq) * D;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            out[c * 4 + e] = Elem<T>::to_store(nparts > 0 ? acc[e] / den : 0.f);
     }
 }
 
 template <typename T, int D>
 static cudaError_t launch_reduce_t(const ReduceArgs &a, cudaStream_t stream) {
-    const size_t smem = sizeof(float) * (size_t)(a.max_parts > 0 ? a.max_parts : 1);
+    const size_t smem = 2 * sizeof(float) * (size_t)(a.max_parts > 0 ? a.max_parts : 1);
     auto kern = split_reduce_kernel<T, D>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
