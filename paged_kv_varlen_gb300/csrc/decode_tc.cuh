@@ -74,8 +74,11 @@ struct DtcCfg {
     static constexpr int PGR = 4;                  // page-id ring of each producer (tiles)
     static constexpr int OFF_PG = OFF_RED + 2 * 2 * 4 * 8 * 4;   // int [2 producers][PGR][16]
     static constexpr int OFF_MISC = OFF_PG + 2 * PGR * 16 * 4;
-    static constexpr int SMEM_BYTES = OFF_MISC + 128 + 1024;   // + alignment slack
     static constexpr int THREADS = 224;            // 4 softmax + K + V producer + MMA warps
+    // batches of at most THREADS requests: their cu_seqlens_q and seq_lens_k,
+    // read once by the work-plan scan
+    static constexpr int OFF_LENS = OFF_MISC + 128;   // int [THREADS + 1] cu, int [THREADS] sl
+    static constexpr int SMEM_BYTES = OFF_LENS + (2 * THREADS + 4) * 4 + 1024;   // + alignment slack
     static constexpr int S_COL = 0;                // two S^T buffers of NP columns
     static constexpr int O_COL = 2 * NP;           // two O^T accumulators of KS * NP columns
     static constexpr int TMEM_COLS = 128;
@@ -161,6 +164,17 @@ __device__ __forceinline__ void dtc_enter(const DecodeTcArgs &a, DtcIter &it, in
         it.pf_cu = __ldg(a.cu_seqlens_q + r + 2);
         it.pf_sl = __ldg(a.seq_lens_k + r + 1);
     }
+}
+
+// dtc_enter with the next request's lengths already known.
+__device__ __forceinline__ void dtc_enter_from(const DecodeTcArgs &a, DtcIter &it, int r, int c0,
+                                               int c1, int sl, int pf_cu, int pf_sl) {
+    it.r = r;
+    it.row = c0;
+    it.cu1 = c1;
+    it.q = dtc_request_from(a, c0, c1, sl);
+    it.pf_cu = pf_cu;
+    it.pf_sl = pf_sl;
 }
 
 __device__ __forceinline__ void dtc_fill(const DecodeTcArgs &a, DtcIter &it) {
@@ -252,6 +266,8 @@ __global__ void __launch_bounds__(224, 1)
     int *plan_rk = reinterpret_cast<int *>(misc + 24);               // first item: r, k
     long long *plan_s = reinterpret_cast<long long *>(misc + 32);    // its start; range end
     long long *scratch = reinterpret_cast<long long *>(misc + 48);   // [7]
+    int *lens_cu = reinterpret_cast<int *>(smem + C::OFF_LENS);      // [S + 1] when S <= THREADS
+    int *lens_sl = lens_cu + C::THREADS + 1;                          // [S]
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -300,41 +316,86 @@ __global__ void __launch_bounds__(224, 1)
     // kernel is this step's scatter)
     if (!a.after_scatter) pdl_wait();
 
-    // ---- this CTA's items: those whose cumulative work starts in [lo, hi)
+    // ---- this CTA's items: those whose cumulative work starts in [lo, hi).
+    // With at most THREADS requests one pass suffices: thread r reads request
+    // r's lengths once (kept in shared memory for the iterators), one block
+    // scan gives every request's cumulative work and the total.
+    const bool one_pass = S <= C::THREADS;
     {
         int64_t acc = 0;
-        for (int r = tid; r < S; r += C::THREADS) acc += dtc_work(dtc_request(a, r), hkv);
+        DtcReq q1 = {0, 0, 0, 0, 0};
+        if (one_pass) {
+            if (tid < S) {
+                const int c0 = a.cu_seqlens_q[tid], c1 = a.cu_seqlens_q[tid + 1];
+                const int sl = a.seq_lens_k[tid];
+                lens_cu[tid] = c0;
+                lens_sl[tid] = sl;
+                if (tid == S - 1) lens_cu[S] = c1;
+                q1 = dtc_request_from(a, c0, c1, sl);
+                acc = dtc_work(q1, hkv);
+            }
+        } else {
+            for (int r = tid; r < S; r += C::THREADS) acc += dtc_work(dtc_request(a, r), hkv);
+        }
         int64_t W;
-        dtc_block_scan<C::THREADS>(acc, scratch, &W);   // (also orders the setup writes)
+        const int64_t incl = dtc_block_scan<C::THREADS>(acc, scratch, &W);   // (orders setup writes)
         const int64_t nb = gridDim.x, b = blockIdx.x;
         const int64_t lo = (W / nb) * b + (W % nb) * b / nb;
         const int64_t hi = (W / nb) * (b + 1) + (W % nb) * (b + 1) / nb;
         if (tid == 0) plan_s[1] = hi;
-        int64_t carry = 0;
-        for (int base = 0; base < S && lo < hi; base += C::THREADS) {
-            const int r = base + tid;
-            const DtcReq q = r < S ? dtc_request(a, r) : DtcReq{0, 0, 0, 0, 0};
-            const int64_t w = dtc_work(q, hkv);
-            int64_t tot;
-            const int64_t E = carry + dtc_block_scan<C::THREADS>(w, scratch, &tot) - w;
-            int k = q.items;
-            int64_t st = 0;
+        // a request holding the CTA's first item: note it, and warm L2 with the
+        // block-table entries of its first tiles (the producers fetch them next)
+        auto candidate = [&](int r, const DtcReq &q, int64_t E, int64_t w, int *k_out,
+                             int64_t *st_out) {
+            *k_out = q.items;
+            *st_out = 0;
             if (q.items > 0 && E < hi && E + w > lo) {
-                k = dtc_first_from(q, hkv, lo - E, &st);
-                if (k < q.items && E + st < hi) atomicMin(found, r);
-            }
-            carry += tot;
-            __syncthreads();
-            const int f = *found;
-            if (f != INT_MAX) {
-                if (r == f) {
-                    plan_rk[0] = r;
-                    plan_rk[1] = k;
-                    plan_s[0] = E + st;
+                *k_out = dtc_first_from(q, hkv, lo - E, st_out);
+                if (*k_out < q.items && E + *st_out < hi) {
+                    atomicMin(found, r);
+                    const int p = *k_out / hkv;
+                    const int kt0 = a.partition_size > 0 ? p * a.partition_size : 0;
+                    const int b0 = kt0 / a.block_size;   // < max_blocks_per_seq: the item has keys
+                    const int32_t *bt = a.block_tables + (int64_t)r * a.max_blocks_per_seq + b0;
+                    prefetch_l2(bt);
+                    if (b0 + 32 < a.max_blocks_per_seq) prefetch_l2(bt + 32);
                 }
-                break;
             }
-            if (carry >= hi) break;
+        };
+        if (one_pass) {
+            int k = 0;
+            int64_t st = 0;
+            if (tid < S && lo < hi) candidate(tid, q1, incl - acc, acc, &k, &st);
+            __syncthreads();
+            if (lo < hi && tid < S && tid == *found) {
+                plan_rk[0] = tid;
+                plan_rk[1] = k;
+                plan_s[0] = incl - acc + st;
+            }
+        } else {
+            int64_t carry = 0;
+            for (int base = 0; base < S && lo < hi; base += C::THREADS) {
+                const int r = base + tid;
+                const DtcReq q = r < S ? dtc_request(a, r) : DtcReq{0, 0, 0, 0, 0};
+                const int64_t w = dtc_work(q, hkv);
+                int64_t tot;
+                const int64_t E = carry + dtc_block_scan<C::THREADS>(w, scratch, &tot) - w;
+                int k;
+                int64_t st;
+                candidate(r, q, E, w, &k, &st);
+                carry += tot;
+                __syncthreads();
+                const int f = *found;
+                if (f != INT_MAX) {
+                    if (r == f) {
+                        plan_rk[0] = r;
+                        plan_rk[1] = k;
+                        plan_s[0] = E + st;
+                    }
+                    break;
+                }
+                if (carry >= hi) break;
+            }
         }
     }
     tc_fence_before();
@@ -347,8 +408,13 @@ __global__ void __launch_bounds__(224, 1)
     it0.k = plan_rk[1];
     it0.s = plan_s[0];
     if (it0.r < S) {
-        dtc_enter(a, it0, it0.r, a.cu_seqlens_q[it0.r], a.cu_seqlens_q[it0.r + 1],
-                  a.seq_lens_k[it0.r]);
+        const int r = it0.r;
+        if (one_pass) {   // the lengths of this request and the next one from shared memory
+            dtc_enter_from(a, it0, r, lens_cu[r], lens_cu[r + 1], lens_sl[r],
+                           r + 1 < S ? lens_cu[r + 2] : 0, r + 1 < S ? lens_sl[r + 1] : 0);
+        } else {
+            dtc_enter(a, it0, r, a.cu_seqlens_q[r], a.cu_seqlens_q[r + 1], a.seq_lens_k[r]);
+        }
         dtc_fill(a, it0);
     }
     auto valid = [&](const DtcIter &x) { return x.r < S && x.s < range_end; };
