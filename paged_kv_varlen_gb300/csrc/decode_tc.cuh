@@ -128,20 +128,6 @@ __device__ __forceinline__ int64_t dtc_work(const DtcReq &q, int hkv) {
     return q.items == 0 ? 0 : ((int64_t)(q.np - 1) * q.wfull + q.wlast) * hkv;
 }
 
-// First item of q whose start (relative to the request) is >= off; *start is
-// that start.  Returns q.items when there is none.
-__device__ __forceinline__ int dtc_first_from(const DtcReq &q, int hkv, int64_t off,
-                                              int64_t *start) {
-    const int64_t nf = (int64_t)(q.np - 1) * hkv;   // items of full partitions
-    const int64_t wf = nf * q.wfull;
-    int64_t k;
-    if (off <= 0) k = 0;
-    else if (off <= wf) k = (off + q.wfull - 1) / q.wfull;
-    else k = nf + (off - wf + q.wlast - 1) / q.wlast;
-    *start = k <= nf ? k * q.wfull : wf + (k - nf) * q.wlast;
-    return (int)(k < q.items ? k : q.items);
-}
-
 // A position in the CTA's sequence of items.  The next request's lengths are
 // loaded when a request is entered, so moving on never waits for memory.
 struct DtcIter {
@@ -177,7 +163,15 @@ __device__ __forceinline__ void dtc_enter_from(const DecodeTcArgs &a, DtcIter &i
     it.pf_sl = pf_sl;
 }
 
-__device__ __forceinline__ void dtc_fill(const DecodeTcArgs &a, DtcIter &it) {
+// The CTA's share of the items cut at tile boundaries: its first item (start
+// s_lo) begins at tile j_lo, and the item starting at s_hi is run up to tile
+// j_hi (exclusive) when j_hi > 0 -- the next CTA runs the rest of it.
+struct DtcCut {
+    int64_t s_lo, s_hi;
+    int j_lo, j_hi;
+};
+
+__device__ __forceinline__ void dtc_fill(const DecodeTcArgs &a, DtcIter &it, const DtcCut &cut) {
     it.p = it.k / a.num_kv_heads;
     it.h = it.k - it.p * a.num_kv_heads;
     if (a.partition_size > 0) {
@@ -188,9 +182,16 @@ __device__ __forceinline__ void dtc_fill(const DecodeTcArgs &a, DtcIter &it) {
         it.k1 = it.q.N;
     }
     it.ntiles = (it.k1 - it.k0 + 127) / 128;
+    const int j1 = it.s == cut.s_hi ? min(it.ntiles, cut.j_hi) : it.ntiles;
+    const int j0 = it.s == cut.s_lo ? cut.j_lo : 0;
+    if (j0 > 0 || j1 < it.ntiles) {
+        it.k1 = min(it.k1, it.k0 + j1 * 128);
+        it.k0 += j0 * 128;
+        it.ntiles = max(0, j1 - j0);
+    }
 }
 
-__device__ __forceinline__ void dtc_next(const DecodeTcArgs &a, DtcIter &it) {
+__device__ __forceinline__ void dtc_next(const DecodeTcArgs &a, DtcIter &it, const DtcCut &cut) {
     it.s += (it.k < (it.q.np - 1) * a.num_kv_heads) ? it.q.wfull : it.q.wlast;
     if (++it.k >= it.q.items) {
         it.k = 0;
@@ -203,7 +204,43 @@ __device__ __forceinline__ void dtc_next(const DecodeTcArgs &a, DtcIter &it) {
             dtc_enter(a, it, r, it.cu1, it.pf_cu, it.pf_sl);
         } while (it.q.items == 0);
     }
-    dtc_fill(a, it);
+    dtc_fill(a, it, cut);
+}
+
+// Where the share boundary at offset `off` (0 <= off < the request's work)
+// cuts request q's items: the upper side starts at item k (returned), tile
+// *j (in [0, tiles of k)), *start being item k's start; k == q.items when the
+// boundary falls at the request's end.  With split partials an item of two or
+// more tiles is cut at the tile boundary nearest to `off` (items weigh five
+// per tile plus three); otherwise an item goes whole to the side its start
+// lies on.
+__device__ __forceinline__ int dtc_cut(const DtcReq &q, int hkv, bool split, int64_t off, int *j,
+                                       int64_t *start) {
+    const int64_t nf = (int64_t)(q.np - 1) * hkv;   // items of full partitions
+    const int64_t wf = nf * q.wfull;
+    int64_t k, st;
+    int w;
+    if (off < wf) {
+        k = off / q.wfull;
+        st = k * q.wfull;
+        w = q.wfull;
+    } else {
+        k = nf + (off - wf) / q.wlast;
+        st = wf + (k - nf) * q.wlast;
+        w = q.wlast;
+    }
+    const int n = (w - 3) / 5;   // the item's tiles
+    int jj;
+    if (split && n >= 2) jj = (int)(((off - st) * 2 * n + w) / (2 * w));   // nearest boundary
+    else jj = off == st ? 0 : n;
+    if (jj >= n && off != st) {   // the whole item stays below the boundary
+        st += w;
+        ++k;
+        jj = 0;
+    }
+    *j = jj;
+    *start = st;
+    return (int)k;
 }
 
 // Inclusive scan over the block's threads; *total = the block's sum.
@@ -262,9 +299,9 @@ __global__ void __launch_bounds__(224, 1)
     uint8_t *misc = smem + C::OFF_MISC;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 8);
-    int *found = reinterpret_cast<int *>(misc + 16);
-    int *plan_rk = reinterpret_cast<int *>(misc + 24);               // first item: r, k
-    long long *plan_s = reinterpret_cast<long long *>(misc + 32);    // its start; range end
+    int *plan_rk = reinterpret_cast<int *>(misc + 16);               // [4] first item r, k; cut item r, k
+    int *plan_j = reinterpret_cast<int *>(misc + 104);               // [2] j_lo, j_hi
+    long long *plan_s = reinterpret_cast<long long *>(misc + 32);    // [2] s_lo, s_hi
     long long *scratch = reinterpret_cast<long long *>(misc + 48);   // [7]
     int *lens_cu = reinterpret_cast<int *>(smem + C::OFF_LENS);      // [S + 1] when S <= THREADS
     int *lens_sl = lens_cu + C::THREADS + 1;                          // [S]
@@ -295,11 +332,14 @@ __global__ void __launch_bounds__(224, 1)
         }
         fence_barrier_init();
         *abort_flag = 0;
-        *found = INT_MAX;
-        plan_rk[0] = S;   // no item unless one is found below
+        plan_rk[0] = S;   // no item unless the share starts inside a request
         plan_rk[1] = 0;
+        plan_rk[2] = -1;   // the item cut at the share's end
+        plan_rk[3] = 0;
         plan_s[0] = 0;
-        plan_s[1] = 0;
+        plan_s[1] = INT64_MAX;   // (the share reaches the batch's end)
+        plan_j[0] = 0;
+        plan_j[1] = 0;
     }
     if (warp == 6) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -316,11 +356,14 @@ __global__ void __launch_bounds__(224, 1)
     // kernel is this step's scatter)
     if (!a.after_scatter) pdl_wait();
 
-    // ---- this CTA's items: those whose cumulative work starts in [lo, hi).
-    // With at most THREADS requests one pass suffices: thread r reads request
-    // r's lengths once (kept in shared memory for the iterators), one block
-    // scan gives every request's cumulative work and the total.
+    // ---- this CTA's share [lo, hi) of the batch's cumulative work, cut at
+    // tile boundaries (see dtc_cut): the request containing lo (resp. hi)
+    // records where the share starts (ends).  With at most THREADS requests
+    // one pass suffices: thread r reads request r's lengths once (kept in
+    // shared memory for the iterators), one block scan gives every request's
+    // cumulative work and the total.
     const bool one_pass = S <= C::THREADS;
+    const bool split = a.partition_size > 0;
     {
         int64_t acc = 0;
         DtcReq q1 = {0, 0, 0, 0, 0};
@@ -342,59 +385,59 @@ __global__ void __launch_bounds__(224, 1)
         const int64_t nb = gridDim.x, b = blockIdx.x;
         const int64_t lo = (W / nb) * b + (W % nb) * b / nb;
         const int64_t hi = (W / nb) * (b + 1) + (W % nb) * (b + 1) / nb;
-        if (tid == 0) plan_s[1] = hi;
-        // a request holding the CTA's first item: note it, and warm L2 with the
-        // block-table entries of its first tiles (the producers fetch them next)
-        auto candidate = [&](int r, const DtcReq &q, int64_t E, int64_t w, int *k_out,
-                             int64_t *st_out) {
-            *k_out = q.items;
-            *st_out = 0;
-            if (q.items > 0 && E < hi && E + w > lo) {
-                *k_out = dtc_first_from(q, hkv, lo - E, st_out);
-                if (*k_out < q.items && E + *st_out < hi) {
-                    atomicMin(found, r);
-                    const int p = *k_out / hkv;
-                    const int kt0 = a.partition_size > 0 ? p * a.partition_size : 0;
-                    const int b0 = kt0 / a.block_size;   // < max_blocks_per_seq: the item has keys
+        // Items are cut between CTAs only when a share holds fewer than ten
+        // full-partition items: whole items then leave the shares up to ~5 %
+        // apart, while a cut starts the next CTA mid-item, out of step with
+        // the others' item boundaries -- measured on GB300 to cost ~8 % of a
+        // GQA decode batch of 4-tile items, and to gain ~3.5 % on a batch of
+        // 8-tile items at 8 items per CTA.
+        const bool cut_items =
+            split && W / nb < 10 * (5 * (int64_t)((a.partition_size + 127) / 128) + 3);
+        // request r (cumulative work E, total w) containing lo or hi; the one
+        // containing lo also warms L2 with the block-table entries of the first
+        // tiles (the producers fetch them next)
+        auto boundaries = [&](int r, const DtcReq &q, int64_t E, int64_t w) {
+            if (q.items == 0 || lo >= hi) return;
+            if (E <= lo && lo < E + w) {
+                int j;
+                int64_t st;
+                const int k = dtc_cut(q, hkv, cut_items, lo - E, &j, &st);
+                plan_rk[0] = r;
+                plan_rk[1] = k;
+                plan_s[0] = E + st;
+                plan_j[0] = j;
+                if (k < q.items) {
+                    const int kt0 = (split ? (k / hkv) * a.partition_size : 0) + j * 128;
+                    const int b0 = kt0 / a.block_size;   // < max_blocks_per_seq: keys there
                     const int32_t *bt = a.block_tables + (int64_t)r * a.max_blocks_per_seq + b0;
                     prefetch_l2(bt);
                     if (b0 + 32 < a.max_blocks_per_seq) prefetch_l2(bt + 32);
                 }
             }
+            if (E <= hi && hi < E + w) {
+                int j;
+                int64_t st;
+                const int k = dtc_cut(q, hkv, cut_items, hi - E, &j, &st);
+                plan_s[1] = E + st;
+                plan_j[1] = j;
+                if (j > 0) {
+                    plan_rk[2] = r;
+                    plan_rk[3] = k;
+                }
+            }
         };
         if (one_pass) {
-            int k = 0;
-            int64_t st = 0;
-            if (tid < S && lo < hi) candidate(tid, q1, incl - acc, acc, &k, &st);
-            __syncthreads();
-            if (lo < hi && tid < S && tid == *found) {
-                plan_rk[0] = tid;
-                plan_rk[1] = k;
-                plan_s[0] = incl - acc + st;
-            }
+            if (tid < S) boundaries(tid, q1, incl - acc, acc);
         } else {
             int64_t carry = 0;
-            for (int base = 0; base < S && lo < hi; base += C::THREADS) {
+            for (int base = 0; base < S && lo < hi && carry <= hi; base += C::THREADS) {
                 const int r = base + tid;
                 const DtcReq q = r < S ? dtc_request(a, r) : DtcReq{0, 0, 0, 0, 0};
                 const int64_t w = dtc_work(q, hkv);
                 int64_t tot;
                 const int64_t E = carry + dtc_block_scan<C::THREADS>(w, scratch, &tot) - w;
-                int k;
-                int64_t st;
-                candidate(r, q, E, w, &k, &st);
+                if (r < S) boundaries(r, q, E, w);
                 carry += tot;
-                __syncthreads();
-                const int f = *found;
-                if (f != INT_MAX) {
-                    if (r == f) {
-                        plan_rk[0] = r;
-                        plan_rk[1] = k;
-                        plan_s[0] = E + st;
-                    }
-                    break;
-                }
-                if (carry >= hi) break;
             }
         }
     }
@@ -402,11 +445,20 @@ __global__ void __launch_bounds__(224, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int64_t range_end = plan_s[1];
+    DtcCut cut;
+    cut.s_lo = plan_s[0];
+    cut.s_hi = plan_s[1];
+    cut.j_lo = plan_j[0];
+    cut.j_hi = plan_j[1];
+    // items: from (s_lo, tile j_lo) up to (s_hi, tile j_hi)
+    const int64_t range_end = cut.s_hi + (cut.j_hi > 0 ? 1 : 0);
     DtcIter it0;
     it0.r = plan_rk[0];
     it0.k = plan_rk[1];
-    it0.s = plan_s[0];
+    it0.s = cut.s_lo;
+    const bool has_work =
+        it0.r < S && (cut.s_lo < cut.s_hi || (cut.s_lo == cut.s_hi && cut.j_lo < cut.j_hi));
+    if (!has_work) it0.r = S;
     if (it0.r < S) {
         const int r = it0.r;
         if (one_pass) {   // the lengths of this request and the next one from shared memory
@@ -415,7 +467,21 @@ __global__ void __launch_bounds__(224, 1)
         } else {
             dtc_enter(a, it0, r, a.cu_seqlens_q[r], a.cu_seqlens_q[r + 1], a.seq_lens_k[r]);
         }
-        dtc_fill(a, it0);
+        if (it0.k >= it0.q.items) {   // the share starts with the next request
+            it0.k = it0.q.items - 1;
+            it0.s -= it0.q.wlast;   // (dtc_next adds the last item's weight back)
+            dtc_next(a, it0, cut);
+        } else {
+            dtc_fill(a, it0, cut);
+        }
+    }
+    // the table of items cut at a share's end (their first part's partial is
+    // in the CTA's extra slot; the reduce merges it).  A CTA whose share holds
+    // no tile writes no partial and records none.
+    if (split && a.cut_tab != nullptr && tid == 0) {
+        const int cr = plan_rk[2], ck = plan_rk[3];
+        a.cut_tab[blockIdx.x] = has_work && cr >= 0 ? make_int4(cr, ck % hkv, ck / hkv, 0)
+                                                    : make_int4(-1, 0, 0, 0);
     }
     auto valid = [&](const DtcIter &x) { return x.r < S && x.s < range_end; };
 
@@ -424,7 +490,7 @@ __global__ void __launch_bounds__(224, 1)
         if (++jj >= x.ntiles) {
             jj = 0;
             ++itx;
-            do dtc_next(a, x);
+            do dtc_next(a, x, cut);
             while (valid(x) && x.ntiles == 0);
         }
     };
@@ -460,8 +526,8 @@ __global__ void __launch_bounds__(224, 1)
         };
         DtcIter cur = it0, la = it0;
         int j = 0, itn = 0, jl = 0, itl = 0;
-        while (valid(cur) && cur.ntiles == 0) dtc_next(a, cur);
-        while (valid(la) && la.ntiles == 0) dtc_next(a, la);
+        while (valid(cur) && cur.ntiles == 0) dtc_next(a, cur, cut);
+        while (valid(la) && la.ntiles == 0) dtc_next(a, la, cut);
         for (int t = 0; t < C::PGR - 1; ++t) {
             fetch_pages(la, jl, t);
             if (valid(la)) adv(la, jl, itl);
@@ -571,7 +637,7 @@ __global__ void __launch_bounds__(224, 1)
             int pv_ob = 0;
             while (valid(cur)) {
                 if (cur.ntiles == 0) {
-                    dtc_next(a, cur);
+                    dtc_next(a, cur, cut);
                     continue;
                 }
                 const int qb = itn & 1;
@@ -618,7 +684,7 @@ __global__ void __launch_bounds__(224, 1)
                     ++gt;
                 }
                 ++itn;
-                dtc_next(a, cur);
+                dtc_next(a, cur, cut);
             }
             if (pv_pending) issue_pv(gt - 1, pv_ob, pv_first, pv_last);
             // every MMA is finished before TMEM is freed (bounded)
@@ -632,7 +698,6 @@ __global__ void __launch_bounds__(224, 1)
         const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
         const float qsc = a.qscale;
         const int Hq = a.num_q_heads;
-        const bool split = a.partition_size > 0;
         DtcIter cur = it0;
         int gt = 0, itn = 0, ie = 0;
         while (valid(cur)) {
@@ -786,16 +851,24 @@ __global__ void __launch_bounds__(224, 1)
             }
             const int hq0 = cur.h * G;
             if (split) {
-                const int64_t slot0 = ((int64_t)cur.r * a.max_parts + cur.p) * Hq + hq0;
+                // the first part of an item cut at the share's end goes to the
+                // CTA's extra slot, every other partial to its partition's slot
+                const bool tail = cur.s == cut.s_hi && cut.j_hi > 0;
+                const int64_t slot0 =
+                    tail ? (int64_t)blockIdx.x * G
+                         : ((int64_t)cur.r * a.max_parts + cur.p) * Hq + hq0;
+                float *po = tail ? a.xpart_o : a.part_o;
+                float *pm = tail ? a.xpart_m : a.part_m;
+                float *pl = tail ? a.xpart_l : a.part_l;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const float inv = L[g] > 0.f ? 1.f / L[g] : 0.f;
 #pragma unroll
                     for (int c = 0; c < C::KS; ++c)
-                        a.part_o[(slot0 + g) * D + c * 128 + t] = o[c][g] * inv;
+                        po[(slot0 + g) * D + c * 128 + t] = o[c][g] * inv;
                     if (t == g) {
-                        a.part_m[slot0 + g] = m_ref[g];
-                        a.part_l[slot0 + g] = L[g];
+                        pm[slot0 + g] = m_ref[g];
+                        pl[slot0 + g] = L[g];
                     }
                 }
             } else {
@@ -821,7 +894,7 @@ __global__ void __launch_bounds__(224, 1)
             }
             if (cur.ntiles > 0) ++itn;
             ++ie;
-            dtc_next(a, cur);
+            dtc_next(a, cur, cut);
         }
     }
 

@@ -134,9 +134,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Split-KV workspace layout: part_o, then part_m, then part_l.
+// Split-KV workspace layout: part_o, part_m, part_l, then the extra partials
+// of items cut between decode CTAs (xpart_o, xpart_m, xpart_l: one slot of up
+// to 8 query heads per CTA) and their table.
 struct SplitLayout {
-    size_t o_bytes, ml_bytes, total;
+    size_t o_bytes, ml_bytes, xo_bytes, xml_bytes, tab_bytes, total;
 };
 
 SplitLayout split_layout(int num_seqs, int max_parts, int num_q_heads, int head_dim) {
@@ -144,7 +146,11 @@ SplitLayout split_layout(int num_seqs, int max_parts, int num_q_heads, int head_
     const size_t units = (size_t)num_seqs * max_parts * num_q_heads;
     L.o_bytes = align256(units * head_dim * sizeof(float));
     L.ml_bytes = align256(units * sizeof(float));
-    L.total = L.o_bytes + 2 * L.ml_bytes;
+    const size_t xunits = (size_t)kMaxDecodeCtas * 8;
+    L.xo_bytes = align256(xunits * head_dim * sizeof(float));
+    L.xml_bytes = align256(xunits * sizeof(float));
+    L.tab_bytes = align256((size_t)kMaxDecodeCtas * sizeof(int4));
+    L.total = L.o_bytes + 2 * L.ml_bytes + L.xo_bytes + 2 * L.xml_bytes + L.tab_bytes;
     return L;
 }
 
@@ -285,14 +291,22 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
                                            dev.sm_count);
     const int max_parts = (P > 0 && max_seqlen_k > 0) ? ceil_div(max_seqlen_k, P) : 1;
     float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
+    float *xpart_o = nullptr, *xpart_m = nullptr, *xpart_l = nullptr;
+    int4 *cut_tab = nullptr;
     if (P > 0 && max_parts > kMaxReduceParts) return PA_ERR_UNSUPPORTED;
     if (P > 0) {
         const SplitLayout L = split_layout(num_seqs, max_parts, num_q_heads, head_dim);
         if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
             return PA_ERR_WORKSPACE;
-        part_o = static_cast<float *>(workspace);
-        part_m = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.o_bytes);
-        part_l = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.o_bytes + L.ml_bytes);
+        char *w = static_cast<char *>(workspace);
+        part_o = reinterpret_cast<float *>(w);
+        part_m = reinterpret_cast<float *>(w + L.o_bytes);
+        part_l = reinterpret_cast<float *>(w + L.o_bytes + L.ml_bytes);
+        w += L.o_bytes + 2 * L.ml_bytes;
+        xpart_o = reinterpret_cast<float *>(w);
+        xpart_m = reinterpret_cast<float *>(w + L.xo_bytes);
+        xpart_l = reinterpret_cast<float *>(w + L.xo_bytes + L.xml_bytes);
+        cut_tab = reinterpret_cast<int4 *>(w + L.xo_bytes + 2 * L.xml_bytes);
     }
 
     // ---- tensor maps over the two caches
@@ -351,6 +365,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
     //    tensor-core decode kernel launched next overlaps it (programmatic
     //    dependent launch) and only its K/V loads wait for it
     const bool tc_decode = dtype == PA_BF16 && (head_dim == 128 || head_dim == 256);
+    int dtc_grid = 0;   // CTAs of the tensor-core decode kernel (0: not launched)
     cudaError_t ce;
     if (fs) {
         const int64_t eb = dtype == PA_F32 ? 4 : 2;
@@ -396,8 +411,14 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         da.box_rows = dbox;
         da.err = dev.err;
         da.after_scatter = fs != nullptr ? 1 : 0;
+        da.xpart_o = xpart_o;
+        da.xpart_m = xpart_m;
+        da.xpart_l = xpart_l;
+        da.cut_tab = cut_tab;
         const int64_t items_max = (int64_t)num_seqs * num_kv_heads * max_parts;
-        const int grid = (int)std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, items_max);
+        const int grid = (int)std::min<int64_t>(
+            std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, kMaxDecodeCtas), items_max);
+        dtc_grid = grid;
         ce = head_dim == 128 ? launch_decode_tc_d128(group, qmap_d, kmap_d, vmap_d, da, grid, s)
                              : launch_decode_tc_d256(group, qmap_d, kmap_d, vmap_d, da, grid, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode_tc launch");
@@ -477,6 +498,12 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         ra.num_q_heads = num_q_heads;
         ra.sinks = sinks;
         ra.meta_before_wait = 1;   // the kernels before it write only out / partials
+        ra.xpart_o = xpart_o;
+        ra.xpart_m = xpart_m;
+        ra.xpart_l = xpart_l;
+        ra.cut_tab = cut_tab;
+        ra.ncut = dtc_grid;   // 0 unless the tensor-core decode kernel ran
+        ra.group = group;
         ce = launch_reduce(e, head_dim, ra, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "split_reduce launch");
     }
@@ -555,6 +582,12 @@ PA_API pa_status pa_split_kv_reduce(void *out, const float *part_out, const floa
     ra.num_q_heads = num_q_heads;
     ra.sinks = sinks;
     ra.meta_before_wait = 0;   // the previous kernel may have written anything
+    ra.xpart_o = nullptr;
+    ra.xpart_m = nullptr;
+    ra.xpart_l = nullptr;
+    ra.cut_tab = nullptr;
+    ra.ncut = 0;
+    ra.group = 1;
     cudaError_t ce = launch_reduce(dtype == PA_F32 ? 4 : 2, head_dim, ra,
                                    static_cast<cudaStream_t>(stream));
     if (ce != cudaSuccess) return cuda_fail(ce, "split_reduce launch");

@@ -78,6 +78,13 @@ struct DecodeTcArgs {
     float *part_l;             // [num_seqs, max_parts, Hq]
     int box_rows;              // rows per K/V TMA box: divides 128, the block and partition sizes
     int *err;                  // device error word
+    // split items cut at a CTA's share end: that CTA's partial of the item's
+    // first part, [grid][G] (o: x D), and the table [grid] of (request, KV
+    // head, partition, 0) of the cut item, request -1 when none
+    float *xpart_o;
+    float *xpart_m;
+    float *xpart_l;
+    int4 *cut_tab;
     // 1: the previous kernel of the stream is the scatter of this step's K/V
     // rows (it writes nothing else the kernel reads): only the K/V loads wait
     // for it.  0: the whole kernel waits for the previous kernel first.
@@ -104,7 +111,17 @@ struct ReduceArgs {
     const float *sinks;
     int meta_before_wait;      // 1: cu_seqlens_q / seq_lens_k / sinks are read before
                                // waiting on the previous kernel (it does not write them)
+    // extra partials of items cut between decode CTAs (ncut = 0: none)
+    const float *xpart_o;      // [ncut][group][D]
+    const float *xpart_m;      // [ncut][group]
+    const float *xpart_l;
+    const int4 *cut_tab;       // [ncut]: (request, KV head, partition, 0), request -1: none
+    int ncut;
+    int group;                 // query heads per KV head
 };
+
+// CTAs of the tensor-core decode kernel at most (one extra partial slot each).
+constexpr int kMaxDecodeCtas = 256;
 
 // Launches `kern` with programmatic stream serialization: it may start while
 // the previous kernel of the stream runs and waits for it with pdl_wait().

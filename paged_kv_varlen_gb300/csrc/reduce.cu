@@ -17,12 +17,14 @@ constexpr int kReduceThreads = 128;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const ReduceArgs a) {
-    extern __shared__ float wsh[];   // [2][max_parts]: partition weights, then maxima
+    extern __shared__ float wsh[];   // [2][max_parts + ncut]: weights, then maxima
     constexpr int LANES = D / 4;                 // float4 slices of one head's row
     constexpr int PG = kReduceThreads / LANES;   // partition groups working in parallel
     __shared__ float red[kReduceThreads / 32];
     __shared__ float Msh, densh;
     __shared__ float4 part[PG > 1 ? PG - 1 : 1][LANES];
+    __shared__ int xslot[kMaxDecodeCtas];   // extra partials of this (request, head)
+    __shared__ int nxs;
     const int r = blockIdx.x;
     const int hq = blockIdx.y;
     const int Hq = a.num_q_heads;
@@ -34,15 +36,34 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
     const int tid = threadIdx.x;
     const float sk2 = a.sinks ? a.sinks[hq] * kLog2e : -INFINITY;
     if (a.meta_before_wait) pdl_wait();    // the partials come from the previous kernel
-    float *msh = wsh + a.max_parts;
+    float *msh = wsh + a.max_parts + a.ncut;
+    // parts of items cut between decode CTAs: extra partials [nparts, nparts + nx)
+    if (tid == 0) nxs = 0;
+    __syncthreads();
+    const int g = a.group > 0 ? hq % a.group : 0;
+    for (int b = tid; b < a.ncut; b += kReduceThreads) {
+        const int4 e = a.cut_tab[b];
+        if (e.x == r && e.y == hq / a.group) xslot[atomicAdd(&nxs, 1)] = b;
+    }
+    __syncthreads();
+    const int nx = nxs;
+    const int ntot = nparts + nx;
 
     // M = max over partitions of m_p, and over the sink logit (m_p and l_p are
     // read together, one pass)
     float mx = -INFINITY;
-    for (int p = tid; p < nparts; p += kReduceThreads) {
-        const int64_t slot = ((int64_t)r * a.max_parts + p) * Hq + hq;
-        const float m = a.part_m[slot];
-        wsh[p] = a.part_l[slot];
+    for (int p = tid; p < ntot; p += kReduceThreads) {
+        float m, l;
+        if (p < nparts) {
+            const int64_t slot = ((int64_t)r * a.max_parts + p) * Hq + hq;
+            m = a.part_m[slot];
+            l = a.part_l[slot];
+        } else {
+            const int64_t xs = (int64_t)xslot[p - nparts] * a.group + g;
+            m = a.xpart_m[xs];
+            l = a.xpart_l[xs];
+        }
+        wsh[p] = l;
         msh[p] = m;
         mx = fmaxf(mx, m);
     }
@@ -57,7 +78,7 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
     __syncthreads();
     const float M = Msh;
     float sum = 0.f;
-    for (int p = tid; p < nparts; p += kReduceThreads) {
+    for (int p = tid; p < ntot; p += kReduceThreads) {
         const float w = wsh[p] * exp2f(msh[p] - M);
         wsh[p] = w;
         sum += w;
@@ -78,11 +99,11 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
     // O = sum_p w_p o_p / den: thread (g, c) sums the float4 slice c over the
     // partitions p = g, g + PG, ... (loads issued four at a time), then the PG
     // groups are added through shared memory
-    const int c = tid % LANES, g = tid / LANES;
+    const int c = tid % LANES, pg = tid / LANES;
     const float *po = a.part_o + ((int64_t)r * a.max_parts * Hq + hq) * D + c * 4;
     const int64_t pstride = (int64_t)Hq * D;   // floats between partitions
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int p = g;
+    int p = pg;
     for (; p + 3 * PG < nparts; p += 4 * PG) {
         float4 o[4];
 #pragma unroll
@@ -97,8 +118,11 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
             acc[3] = fmaf(w, o[u].w, acc[3]);
         }
     }
-    for (; p < nparts; p += PG) {
-        const float4 o = *reinterpret_cast<const float4 *>(po + (int64_t)p * pstride);
+    for (; p < ntot; p += PG) {
+        const float *src = p < nparts
+                               ? po + (int64_t)p * pstride
+                               : a.xpart_o + ((int64_t)xslot[p - nparts] * a.group + g) * D + c * 4;
+        const float4 o = *reinterpret_cast<const float4 *>(src);
         const float w = wsh[p];
         acc[0] = fmaf(w, o.x, acc[0]);
         acc[1] = fmaf(w, o.y, acc[1]);
@@ -106,9 +130,9 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
         acc[3] = fmaf(w, o.w, acc[3]);
     }
     if (PG > 1) {
-        if (g > 0) part[g - 1][c] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        if (pg > 0) part[pg - 1][c] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         __syncthreads();
-        if (g == 0) {
+        if (pg == 0) {
 #pragma unroll
             for (int k = 0; k < PG - 1; ++k) {
                 const float4 o = part[k][c];
@@ -119,7 +143,7 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
             }
         }
     }
-    if (g == 0) {
+    if (pg == 0) {
         T *out = reinterpret_cast<T *>(a.out) + ((int64_t)c0 * Hq + hq) * D;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -129,7 +153,7 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
 
 template <typename T, int D>
 static cudaError_t launch_reduce_t(const ReduceArgs &a, cudaStream_t stream) {
-    const size_t smem = 2 * sizeof(float) * (size_t)(a.max_parts > 0 ? a.max_parts : 1);
+    const size_t smem = 2 * sizeof(float) * (size_t)((a.max_parts > 0 ? a.max_parts : 1) + a.ncut);
     auto kern = split_reduce_kernel<T, D>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -62,15 +62,25 @@ class DeviceWorkload:
         pa.pa_reshape_and_cache(self.new_k, self.new_v, self.key_cache, self.value_cache,
                                 self.slot_mapping)
 
+    def poisoned_workspace(self, partition_size):
+        """A workspace of the size the call needs, every byte 0xFF (NaN as fp32):
+        its contents need no initialisation, so no result may depend on them."""
+        w = self.w
+        n = pa.pa_varlen_attention_workspace_size(w.num_seqs, w.max_seqlen_k, w.num_q_heads,
+                                                  w.head_dim, partition_size)
+        return torch.full((max(n, 16),), 0xFF, dtype=torch.uint8, device="cuda")
+
     def attention(self, partition_size=None, workspace=None, sinks="default", out=None):
         w = self.w
         out = self.out if out is None else out
+        P = w.partition_size if partition_size is None else partition_size
+        if workspace is None:
+            workspace = self.poisoned_workspace(P)
         pa.pa_varlen_attention(
             out, self.q, self.key_cache, self.value_cache, self.cu_seqlens_q, self.seq_lens_k,
             self.block_tables, max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k,
             scale=w.scale, sinks=self.sinks if sinks == "default" else sinks, causal=w.causal,
-            partition_size=w.partition_size if partition_size is None else partition_size,
-            workspace=workspace)
+            partition_size=P, workspace=workspace)
         return out
 
     def step(self, **kw):
@@ -81,12 +91,13 @@ class DeviceWorkload:
         """The same step through pa_scatter_and_attend (one call)."""
         w = self.w
         out = self.out if out is None else out
+        P = w.partition_size if partition_size is None else partition_size
         pa.pa_scatter_and_attend(
             self.new_k, self.new_v, self.slot_mapping, out, self.q, self.key_cache,
             self.value_cache, self.cu_seqlens_q, self.seq_lens_k, self.block_tables,
             max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k, scale=w.scale,
-            sinks=self.sinks, causal=w.causal,
-            partition_size=w.partition_size if partition_size is None else partition_size)
+            sinks=self.sinks, causal=w.causal, partition_size=P,
+            workspace=self.poisoned_workspace(P))
         return out
 
 

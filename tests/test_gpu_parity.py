@@ -48,6 +48,17 @@ def test_decode_partitions(P, dtype):
     check_step(w)
 
 
+@pytest.mark.parametrize("with_sinks", [False, True])
+def test_decode_item_split_across_many_ctas(with_sinks):
+    """One 65536-key partition next to 100 one-tile requests: the decode grid
+    balances tiles, so that partition is cut between dozens of CTAs, whose
+    partials the reduce merges (kwkr.cn trick 4: split partials + one reduce)."""
+    prior = np.array([65535] + [127] * 100, dtype=np.int64)
+    w = wl.build("split_across_ctas", wl.BF16, 4, 1, 128, 16, prior, np.ones(101, np.int64),
+                 seed=101, partition_size=65536, with_sinks=with_sinks, pool_slack=1.2)
+    check_step(w)
+
+
 def test_non_causal_rows():
     w = wl.random_small(78, dtype=wl.F32, num_seqs=4, head_dim=64, max_prior=100, max_q=9,
                         causal=False)
