@@ -56,8 +56,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM bytes (read + write) of one paged_decode_tc_kernel launch on workload 1,
 # from ncu (dram__bytes_read.sum + dram__bytes_write.sum); valid while the
 # kernel sources hash to the value below.
-NCU_TRAFFIC = {"sources_sha256": "c1612917ff17e6f8bd1817656164f235fa823dfd38613e38805e8e363c602961",
-               "bytes_per_launch": 526311424 + 5195008, "workload": 1}
+NCU_TRAFFIC = {"sources_sha256": "8521532878800c98af6f85ecf0d8336123f4124ab4227594bfb1906dad4497b8",
+               "bytes_per_launch": 526379776 + 5281536, "workload": 1}
 
 
 def kernel_sources_hash() -> str:
