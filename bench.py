@@ -403,22 +403,25 @@ def run_ours(args, rank, world, local):
     step_s = elapsed_s / steps
     value, unit = metric_value(kind, work, step_s, world)
 
-    # ---------------- end to end through the public API with host buffers
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    h_q, h_nk, h_nv, h_sm = pin(q), pin(nk), pin(nv), pin(sm)
-    h_cu, h_sl, h_bt = pin(cu), pin(sl), pin(bt)
+    # ---------------- end to end through the public API with host buffers: the
+    # step's inputs packed in one pinned staging buffer (one host-to-device
+    # copy), the output read back
+    from paged_kv_varlen_gb300.staging import StepStaging
+    stage = StepStaging({"q": q, "new_k": nk, "new_v": nv, "slot_mapping": sm,
+                         "cu_seqlens_q": cu, "seq_lens_k": sl, "block_tables": bt}, device)
+    for name, t in (("q", q), ("new_k", nk), ("new_v", nv), ("slot_mapping", sm),
+                    ("cu_seqlens_q", cu), ("seq_lens_k", sl), ("block_tables", bt)):
+        stage.host[name].copy_(t.cpu())
+    dv = stage.dev
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    d_q, d_nk, d_nv, d_sm = (torch.empty_like(t) for t in (q, nk, nv, sm))
-    d_cu, d_sl, d_bt = (torch.empty_like(t) for t in (cu, sl, bt))
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_nk, h_nv, h_sm, h_cu, h_sl, h_bt))
+    h2d = stage.nbytes
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        for d, h in ((d_q, h_q), (d_nk, h_nk), (d_nv, h_nv), (d_sm, h_sm), (d_cu, h_cu),
-                     (d_sl, h_sl), (d_bt, h_bt)):
-            d.copy_(h, non_blocking=True)
-        scatter(d_nk, d_nv, d_sm)
-        attend(d_q, d_cu, d_sl, d_bt, k_in=d_nk, v_in=d_nv, s_in=d_sm)
+        stage.upload()
+        scatter(dv["new_k"], dv["new_v"], dv["slot_mapping"])
+        attend(dv["q"], dv["cu_seqlens_q"], dv["seq_lens_k"], dv["block_tables"],
+               k_in=dv["new_k"], v_in=dv["new_v"], s_in=dv["slot_mapping"])
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):

@@ -7,8 +7,9 @@ CUDA sources in ``csrc/``; ``binding`` marshals torch tensors into its calls:
   pa_varlen_attention    attention over packed query rows and paged K/V
   pa_split_kv_reduce     merge split-KV partials (log2-space max / exp-sum)
 
-Importing the package does not load the library; the first call does, and it
+``staging`` packs a step's input arrays into one pinned host buffer (one
+host-to-device copy per step).  Importing the package does not load the library; the first call does, and it
 raises if the library is missing -- there is no CPU fallback.
 """
 
-__all__ = ["binding", "workloads"]
+__all__ = ["binding", "staging", "workloads"]

@@ -352,3 +352,38 @@ def test_zero_and_negative_scale(scale, dtype):
                         num_kv_heads=2, max_prior=400, max_q=6, with_sinks=True)
     w.scale = scale
     check_step(w)
+
+
+def test_step_staging_one_copy_matches_separate_inputs():
+    """StepStaging: the step's inputs packed in one pinned buffer and uploaded in
+    one copy give the same caches and output as separately copied inputs."""
+    from paged_kv_varlen_gb300.staging import StepStaging
+    w = wl.random_small(99, dtype=wl.BF16, num_seqs=9, num_q_heads=8, num_kv_heads=2,
+                        head_dim=128, max_prior=900, max_q=4, with_sinks=True)
+    ref = DeviceWorkload(w)
+    ref.fused_step(partition_size=256)
+    got = DeviceWorkload(w)
+    names = {"q": got.q, "new_k": got.new_k, "new_v": got.new_v,
+             "slot_mapping": got.slot_mapping, "cu_seqlens_q": got.cu_seqlens_q,
+             "seq_lens_k": got.seq_lens_k, "block_tables": got.block_tables}
+    stage = StepStaging(names, got.q.device)
+    for n, t in names.items():
+        stage.host[n].copy_(t.cpu())
+    stage.upload()
+    torch.cuda.synchronize()
+    for n, t in names.items():
+        assert stage.dev[n].data_ptr() % 256 == 0
+        assert torch.equal(stage.dev[n].view(torch.uint8) if t.dtype == torch.bfloat16
+                           else stage.dev[n], t.view(torch.uint8) if t.dtype == torch.bfloat16
+                           else t)
+    d = stage.dev
+    out = torch.empty_like(got.q)
+    pa.pa_scatter_and_attend(
+        d["new_k"], d["new_v"], d["slot_mapping"], out, d["q"], got.key_cache, got.value_cache,
+        d["cu_seqlens_q"], d["seq_lens_k"], d["block_tables"], max_seqlen_q=w.max_seqlen_q,
+        max_seqlen_k=w.max_seqlen_k, scale=w.scale, sinks=got.sinks, causal=w.causal,
+        partition_size=256, workspace=got.poisoned_workspace(256))
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    assert torch.equal(dev_bits_t(ref.key_cache), dev_bits_t(got.key_cache))
+    assert torch.equal(dev_bits_t(ref.out), dev_bits_t(out))
