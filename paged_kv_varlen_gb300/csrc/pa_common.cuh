@@ -102,14 +102,6 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 
 // ---------------------------------------------------------------- cp.async
-// 16-byte asynchronous global -> shared copy (bypasses L1).  src_bytes = 0
-// reads nothing and writes 16 zero bytes.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes,
-                                           uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
-                 "l"(src), "r"(src_bytes), "l"(policy)
-                 : "memory");
-}
 // 4-byte asynchronous global -> shared copy (through L1).
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
