@@ -157,7 +157,7 @@ SplitLayout split_layout(int num_seqs, int max_parts, int num_q_heads, int head_
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 // This step's K/V rows for pa_scatter_and_attend (one per query row).
-struct FusedScatter {
+struct StepScatter {
     const void *key;
     const void *value;
     int64_t stride;                 // elements between tokens
@@ -255,7 +255,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
                                 int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                                 float scale, const float *sinks, int causal, int partition_size,
                                 void *workspace, size_t workspace_bytes, pa_dtype dtype,
-                                void *stream, const FusedScatter *fs) {
+                                void *stream, const StepScatter *fs) {
     // ---- host-side checks (nothing is launched if one fails)
     if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
     if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
@@ -546,7 +546,7 @@ PA_API pa_status pa_scatter_and_attend(const void *key, const void *value, int64
     const uintptr_t e = dtype == PA_F32 ? 4 : 2;
     if (((reinterpret_cast<uintptr_t>(key) | reinterpret_cast<uintptr_t>(value)) % e) != 0)
         return PA_ERR_INVALID_ARG;
-    const FusedScatter fs = {key, value, kv_token_stride, slot_mapping};
+    const StepScatter fs = {key, value, kv_token_stride, slot_mapping};
     return attention_impl(out, q, key_cache, value_cache, cu_seqlens_q, seq_lens_k, block_tables,
                           max_blocks_per_seq, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,

@@ -161,8 +161,9 @@ def test_block_size_144_as_nine_16_token_pages():
 
 
 FUSED = [
-    # (name, workload factory): decode only and mixed steps take the fused path
-    # (bf16, D = 128 / 256); fp32 and D = 64 take the scatter kernel first
+    # (name, workload factory): decode-only and mixed steps; with bf16 at D = 128 /
+    # 256 the decode kernel is launched while the scatter runs (only its K/V
+    # loads wait for it), fp32 and D = 64 run the kernels one after the other
     ("decode-bf16-D128", lambda: wl.random_small(91, dtype=wl.BF16, num_seqs=6, head_dim=128,
                                                   num_q_heads=8, num_kv_heads=2, max_prior=1400,
                                                   max_q=1, with_sinks=True)),
