@@ -14,6 +14,7 @@
 namespace pa {
 
 constexpr int kReduceThreads = 128;
+static_assert(kMaxDecodeCtas % kReduceThreads == 0, "cut-table rounds");
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const ReduceArgs a) {
@@ -24,7 +25,7 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
     __shared__ float Msh, densh;
     __shared__ float4 part[PG > 1 ? PG - 1 : 1][LANES];
     __shared__ int xslot[kMaxDecodeCtas];   // extra partials of this (request, head)
-    __shared__ int nxs;
+    __shared__ int xcount[kMaxDecodeCtas / 32];   // hits per (round, warp)
     const int r = blockIdx.x;
     const int hq = blockIdx.y;
     const int Hq = a.num_q_heads;
@@ -37,16 +38,38 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
     const float sk2 = a.sinks ? a.sinks[hq] * kLog2e : -INFINITY;
     if (a.meta_before_wait) pdl_wait();    // the partials come from the previous kernel
     float *msh = wsh + a.max_parts + a.ncut;
-    // parts of items cut between decode CTAs: extra partials [nparts, nparts + nx)
-    if (tid == 0) nxs = 0;
-    __syncthreads();
+    // parts of items cut between decode CTAs: extra partials [nparts, nparts + nx),
+    // listed in cut-table order (ballots and per-warp counts, no atomics), so
+    // the partials are always summed in the same order: bit-reproducible
     const int g = a.group > 0 ? hq % a.group : 0;
-    for (int b = tid; b < a.ncut; b += kReduceThreads) {
-        const int4 e = a.cut_tab[b];
-        if (e.x == r && e.y == hq / a.group) xslot[atomicAdd(&nxs, 1)] = b;
+    constexpr int RND = kMaxDecodeCtas / kReduceThreads;
+    constexpr int NW = kReduceThreads / 32;
+    const int lane = tid & 31, wid = tid >> 5;
+    uint32_t bal[RND];
+#pragma unroll
+    for (int k = 0; k < RND; ++k) {
+        const int b = k * kReduceThreads + tid;
+        bool hit = false;
+        if (b < a.ncut) {
+            const int4 e = a.cut_tab[b];
+            hit = e.x == r && e.y == hq / a.group;
+        }
+        bal[k] = __ballot_sync(0xffffffffu, hit);
+        if (lane == 0) xcount[k * NW + wid] = __popc(bal[k]);
     }
     __syncthreads();
-    const int nx = nxs;
+    int nx = 0;
+#pragma unroll
+    for (int k = 0; k < RND; ++k) {
+        int before = 0;   // hits at lower cut-table indices
+#pragma unroll
+        for (int q = 0; q < RND * NW; ++q) before += q < k * NW + wid ? xcount[q] : 0;
+        if ((bal[k] >> lane) & 1u)
+            xslot[before + __popc(bal[k] & ((1u << lane) - 1u))] = k * kReduceThreads + tid;
+    }
+#pragma unroll
+    for (int q = 0; q < RND * NW; ++q) nx += xcount[q];
+    __syncthreads();
     const int ntot = nparts + nx;
 
     // M = max over partitions of m_p, and over the sink logit (m_p and l_p are
