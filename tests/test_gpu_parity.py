@@ -59,6 +59,20 @@ def test_decode_item_split_across_many_ctas(with_sinks):
     check_step(w)
 
 
+def test_split_merge_is_bit_reproducible():
+    """A partition cut across dozens of CTAs leaves many extra partials per
+    head; the reduce merges them in a fixed (cut-table) order, so two runs
+    give identical bits."""
+    prior = np.array([65535] + [127] * 100, dtype=np.int64)
+    w = wl.build("split_across_ctas", wl.BF16, 4, 1, 128, 16, prior, np.ones(101, np.int64),
+                 seed=101, partition_size=65536, with_sinks=True, pool_slack=1.2)
+    first = _run(w)
+    second = _run(w)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    assert torch.equal(dev_bits_t(first.out), dev_bits_t(second.out))
+
+
 def test_non_causal_rows():
     w = wl.random_small(78, dtype=wl.F32, num_seqs=4, head_dim=64, max_prior=100, max_q=9,
                         causal=False)
