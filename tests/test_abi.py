@@ -102,6 +102,39 @@ def test_attention_argument_checks_return_before_any_launch(lib, over, status):
     assert _call_attention(lib, **over) == status
 
 
+def _call_scatter_and_attend(lib, **over):
+    args = dict(key=16, value=16, stride=128, slots=16, T=2, out=16, q=16, kc=16, vc=16, cu=16,
+                sl=16, bt=16, mbps=4, S=2, total_q=2, mq=1, mk=40, Hq=4, Hkv=2, D=64, bs=16,
+                nb=16, scale=0.125, sinks=None, causal=1, P=0, ws=None, ws_bytes=0, dtype=0,
+                stream=None)
+    args.update(over)
+    v = ctypes.c_void_p
+    return lib.pa_scatter_and_attend(
+        v(args["key"]), v(args["value"]), args["stride"], v(args["slots"]), args["T"],
+        v(args["out"]), v(args["q"]), v(args["kc"]), v(args["vc"]), v(args["cu"]), v(args["sl"]),
+        v(args["bt"]), args["mbps"], args["S"], args["total_q"], args["mq"], args["mk"],
+        args["Hq"], args["Hkv"], args["D"], args["bs"], args["nb"], args["scale"],
+        args["sinks"], args["causal"], args["P"], args["ws"], args["ws_bytes"], args["dtype"],
+        args["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(T=3), 1),                    # one new K/V row per query row
+    (dict(stride=100), 1),             # token stride < H_kv * D
+    (dict(key=0), 1),                  # null key rows
+    (dict(slots=0), 1),                # null slot mapping
+    (dict(key=17, dtype=1), 1),        # bf16 key rows not 2-byte aligned
+    (dict(dtype=5), 1),                # unknown dtype
+    (dict(Hq=18, Hkv=2, stride=256), 2),   # the attention's own checks follow: group of 9
+    (dict(D=96, stride=192), 2),       # head_dim not compiled
+    (dict(T=0, total_q=0), 0),         # nothing to do
+])
+def test_scatter_and_attend_argument_checks(lib, over, status):
+    """The step call checks its scatter arguments, then the attention's, all
+    before any CUDA call."""
+    assert _call_scatter_and_attend(lib, **over) == status
+
+
 def test_scatter_argument_checks(lib):
     v = ctypes.c_void_p
     f = lib.pa_reshape_and_cache
