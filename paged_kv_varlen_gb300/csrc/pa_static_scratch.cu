@@ -62,6 +62,13 @@ PA_API pa_status pa_varlen_attention_static_scratch(
     int num_q_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
     float scale, const float *sinks, int causal, int partition_size, pa_dtype dtype,
     void *stream) {
+    // no rows: the attention call's own checks and its PA_OK, with no device query
+    if (total_q == 0)
+        return pa_varlen_attention(out, q, key_cache, value_cache, cu_seqlens_q, seq_lens_k,
+                                   block_tables, max_blocks_per_seq, num_seqs, total_q,
+                                   max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads,
+                                   head_dim, block_size, num_blocks, scale, sinks, causal,
+                                   partition_size, nullptr, 0, dtype, stream);
     if (total_q > 0 && num_seqs > 0 && num_q_heads > 0 && head_dim > 0 && num_kv_heads > 0) {
         // The scratch this call's split plan needs (the plan depends on the
         // device's SM count, read without allocating anything).

@@ -135,6 +135,20 @@ def test_scatter_and_attend_argument_checks(lib, over, status):
     assert _call_scatter_and_attend(lib, **over) == status
 
 
+def test_static_scratch_with_no_rows_needs_no_device(lib):
+    """No rows: PA_OK (or the dtype error) before any device query, as for
+    pa_varlen_attention itself."""
+    v = ctypes.c_void_p
+    f = lib.pa_varlen_attention_static_scratch
+    f.restype = ctypes.c_int
+    f.argtypes = [v, v, v, v, v, v, v, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int64, ctypes.c_float, v, ctypes.c_int, ctypes.c_int, ctypes.c_int, v]
+    base = [v(16)] * 7 + [4, 2, 0, 1, 40, 4, 2, 64, 16, 16, 0.125, None, 1, 0]
+    assert f(*base, 0, None) == 0
+    assert f(*base, 7, None) == 1
+
+
 def test_scatter_argument_checks(lib):
     v = ctypes.c_void_p
     f = lib.pa_reshape_and_cache
