@@ -56,7 +56,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM bytes (read + write) of one paged_decode_tc_kernel launch on workload 1,
 # from ncu (dram__bytes_read.sum + dram__bytes_write.sum); valid while the
 # kernel sources hash to the value below.
-NCU_TRAFFIC = {"sources_sha256": "6df86a990c1f20d742bd31e09076d81b0451f71041e6582c9cd8804d08f7a5a6",
+NCU_TRAFFIC = {"sources_sha256": "762a3d5dd94725543cbd07b956d98f6bd4e443cec73bf4cf281bb576196db805",
                "bytes_per_launch": 526379776 + 5281536, "workload": 1}
 
 
