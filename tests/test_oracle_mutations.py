@@ -3,8 +3,9 @@
 Each case plants one mistake in a copy of oracle/pa_oracle.c -- a wrong GQA
 head map, a causal limit off by one, a wrong slot inside a page, a dropped
 score scale, a sink with the wrong sign, values read from the key cache, a
-reduce that forgets the exp-sum weights, a scatter into the wrong slot or of
-padding tokens -- rebuilds that copy in a temporary tree and runs the pins
+split partial whose max is not in the log2 domain, a reduce that forgets the
+exp-sum weights, a scatter into the wrong slot or of padding tokens --
+rebuilds that copy in a temporary tree and runs the pins
 (tests/test_oracle_pins.py) against it: at least one pin must fail.  The
 repository's own oracle is not touched.
 """
@@ -37,6 +38,9 @@ MUTATIONS = [
     ("values_from_key_cache",
      "for (int d = 0; d < D; ++d) o[d] += p * elem(a->value_cache, vo + d, a->dtype);",
      "for (int d = 0; d < D; ++d) o[d] += p * elem(a->key_cache, vo + d, a->dtype);"),
+    ("partial_max_natural_units",
+     "double t2 = scale * dot * log2e;",
+     "double t2 = scale * dot;"),
     ("reduce_weight",
      "double w = PART(part_l, slot) * exp2(PART(part_m, slot) - M);",
      "double w = exp2(PART(part_m, slot) - M);"),

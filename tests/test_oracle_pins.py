@@ -328,6 +328,39 @@ def test_split_kv_equals_no_split(P):
     assert np.max(np.abs(out - ref)) < 1e-12
 
 
+def test_split_partials_single_key_closed_form_and_bounds():
+    """Trick 4's partials by their definition: m_p is the partition's log2-domain
+    max, so the largest term is 2^0 = 1 and 1 <= l_p <= (keys in the partition);
+    a partition holding one key has l_p = 1 exactly and o_p = that key's value row.
+    (The combined output alone cannot pin the units of m_p: any reference max
+    with its matching exp-sum combines to the same result.)"""
+    P = 64
+    prior = np.array([2 * P, P, 3 * P - 1, 0], dtype=np.int64)   # N = 2P+1, P+1, 3P, 1
+    w = wl.build("partials", wl.F32, 4, 2, 32, 16, prior, np.ones(4, np.int64), seed=31,
+                 partition_size=P)
+    kc, vc = w.pool_with_new_tokens()
+    max_parts = int(math.ceil(w.max_seqlen_k / P))
+    po, pm, pl = oracle.split_partials(w.q, kc, vc, w.cu_seqlens_q, w.seq_lens_k, w.block_tables,
+                                       dtype=w.dtype, num_q_heads=w.num_q_heads,
+                                       num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                                       block_size=w.block_size, scale=w.scale,
+                                       partition_size=P, max_parts=max_parts)
+    v_all = wl.to_f64(w.v_ctx, w.dtype)
+    single = 0
+    for r in range(w.num_seqs):
+        N = int(w.seq_lens[r])
+        for p in range((N + P - 1) // P):
+            n_p = min(N, (p + 1) * P) - p * P
+            for h in range(w.num_q_heads):
+                assert 1.0 - 1e-12 <= pl[r, p, h] <= n_p + 1e-12
+                if n_p == 1:
+                    assert pl[r, p, h] == 1.0
+                    v = v_all[w.ctx_offsets[r] + p * P, h // w.group]
+                    assert np.max(np.abs(po[r, p, h] - v)) < 1e-12
+                    single += 1
+    assert single == 3 * w.num_q_heads
+
+
 def test_scatter_is_byte_exact_and_keeps_untouched_slots():
     w = wl.random_small(23, dtype=wl.BF16, num_seqs=4, max_q=7)
     sm = w.slot_mapping.copy()
