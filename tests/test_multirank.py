@@ -49,3 +49,18 @@ def test_timing_is_max_over_ranks_and_work_is_summed():
         assert worst == 2.0                       # max over ranks
         assert unit == "GB/s"
         assert abs(value - 2 * 100.0 / 2.0) < 1e-9   # both ranks' bytes / slowest time
+
+
+def test_reference_arm_runs_on_rank_0_only():
+    """Under a multi-rank launch the oracle arm runs on rank 0 alone: another
+    rank exits 0 at once, printing nothing and doing no work."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1",
+               MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()))
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2",
+                          "--steps", "1", "--warmup", "3"],
+                         cwd=root, env=env, capture_output=True, text=True, timeout=120)
+    assert res.returncode == 0, res.stderr[-2000:]
+    assert res.stdout.strip() == ""
