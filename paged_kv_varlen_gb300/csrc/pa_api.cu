@@ -245,6 +245,55 @@ PA_API pa_status pa_reshape_and_cache(const void *key, const void *value, int64_
     return PA_OK;
 }
 
+namespace pa {
+
+// Host-side argument checks of pa_varlen_attention (and of every call built on
+// it); each failure names its reason in pa_last_error_string().
+pa_status check_attention_args(const void *out, const void *q, const void *key_cache,
+                               const void *value_cache, const int32_t *cu_seqlens_q,
+                               const int32_t *seq_lens_k, const int32_t *block_tables,
+                               int max_blocks_per_seq, int num_seqs, int64_t total_q,
+                               int max_seqlen_q, int max_seqlen_k, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                               const float *sinks, int partition_size, pa_dtype dtype) {
+    auto fail = [](pa_status st, const char *why) {
+        snprintf(g_last_error, sizeof g_last_error, "%s", why);
+        return st;
+    };
+    if (dtype != PA_F32 && dtype != PA_BF16) return fail(PA_ERR_INVALID_ARG, "unknown dtype");
+    if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+        return fail(PA_ERR_INVALID_ARG, "negative size");
+    if (total_q == 0) return PA_OK;
+    if (num_seqs == 0) return fail(PA_ERR_INVALID_ARG, "query rows but no request");
+    if (!out || !q || !key_cache || !value_cache || !cu_seqlens_q || !seq_lens_k || !block_tables)
+        return fail(PA_ERR_INVALID_ARG, "null pointer");
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+    if (max_blocks_per_seq <= 0 || num_blocks <= 0 || block_size <= 0)
+        return fail(PA_ERR_INVALID_ARG, "block table and pool sizes must be positive");
+    if (partition_size < -1 || (partition_size > 0 && partition_size % 32 != 0))
+        return fail(PA_ERR_INVALID_ARG,
+                    "partition_size must be -1, 0 or a positive multiple of 32");
+    if (num_q_heads / num_kv_heads > 8)
+        return fail(PA_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+    if (block_size % 8 != 0 || block_size > 1024)
+        return fail(PA_ERR_UNSUPPORTED, "block_size must be a multiple of 8 up to 1024");
+    if (num_seqs > 65535 || num_kv_heads > 65535)
+        return fail(PA_ERR_UNSUPPORTED, "more than 65535 requests or KV heads");
+    if (num_blocks * block_size > 0x7fffffffLL ||
+        (int64_t)max_blocks_per_seq * block_size > 0x7fffffffLL || total_q > 0x7fffffffLL)
+        return fail(PA_ERR_UNSUPPORTED, "pool, block table or batch beyond 2^31 rows");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+        return fail(PA_ERR_INVALID_ARG, "q, out and the caches must be 16-byte aligned");
+    if (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3))
+        return fail(PA_ERR_INVALID_ARG, "sinks must be 4-byte aligned");
+    return PA_OK;
+}
+
+}  // namespace pa
+
 // The attention call; with `fs`, this step's K/V rows are scattered first --
 // inside the tensor-core decode kernel when it runs, else by the scatter kernel.
 static pa_status attention_impl(void *out, const void *q, const void *key_cache,
@@ -257,32 +306,17 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
                                 void *workspace, size_t workspace_bytes, pa_dtype dtype,
                                 void *stream, const StepScatter *fs) {
     // ---- host-side checks (nothing is launched if one fails)
-    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
-    if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
-        return PA_ERR_INVALID_ARG;
+    pa_status st = check_attention_args(out, q, key_cache, value_cache, cu_seqlens_q, seq_lens_k,
+                                        block_tables, max_blocks_per_seq, num_seqs, total_q,
+                                        max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads,
+                                        head_dim, block_size, num_blocks, sinks, partition_size,
+                                        dtype);
+    if (st != PA_OK) return st;
     if (total_q == 0) return PA_OK;
-    if (num_seqs == 0) return PA_ERR_INVALID_ARG;
-    if (!out || !q || !key_cache || !value_cache || !cu_seqlens_q || !seq_lens_k || !block_tables)
-        return PA_ERR_INVALID_ARG;
-    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
-        return PA_ERR_INVALID_ARG;
-    if (max_blocks_per_seq <= 0 || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
-    if (partition_size < -1 || (partition_size > 0 && partition_size % 32 != 0))
-        return PA_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
-    if (group > 8) return PA_ERR_UNSUPPORTED;
-    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
-    if (block_size % 8 != 0 || block_size > 1024) return PA_ERR_UNSUPPORTED;
-    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
-    if (num_blocks * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    if ((int64_t)max_blocks_per_seq * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    if (total_q > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
-        return PA_ERR_INVALID_ARG;
-    if (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3)) return PA_ERR_INVALID_ARG;
 
     DeviceInfo dev;
-    pa_status st = device_info(&dev);
+    st = device_info(&dev);
     if (st != PA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -293,11 +327,21 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
     float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
     float *xpart_o = nullptr, *xpart_m = nullptr, *xpart_l = nullptr;
     int4 *cut_tab = nullptr;
-    if (P > 0 && max_parts > kMaxReduceParts) return PA_ERR_UNSUPPORTED;
+    if (P > 0 && max_parts > kMaxReduceParts) {
+        snprintf(g_last_error, sizeof g_last_error,
+                 "%d split-KV partitions per request, at most %d", max_parts, kMaxReduceParts);
+        return PA_ERR_UNSUPPORTED;
+    }
     if (P > 0) {
         const SplitLayout L = split_layout(num_seqs, max_parts, num_q_heads, head_dim);
-        if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
+        if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) {
+            snprintf(g_last_error, sizeof g_last_error,
+                     "this call needs %zu bytes of 16-byte aligned workspace (split-KV "
+                     "partition %d, %d partitions per request); %zu given%s",
+                     L.total, P, max_parts, workspace ? workspace_bytes : (size_t)0,
+                     workspace && !aligned16(workspace) ? " (misaligned)" : "");
             return PA_ERR_WORKSPACE;
+        }
         char *w = static_cast<char *>(workspace);
         part_o = reinterpret_cast<float *>(w);
         part_m = reinterpret_cast<float *>(w + L.o_bytes);
@@ -457,26 +501,15 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         ta.causal = causal ? 1 : 0;
         ta.box_rows = tc_box;
         ta.err = dev.err;
-        auto launch_tc = [&](bool paired, dim3 grid) -> cudaError_t {
-            switch (head_dim) {
-                case 64: return launch_prefill_tc_d64(group, paired, qmap, kmap_tc, vmap_tc, ta,
-                                                      grid, s);
-                case 128: return launch_prefill_tc_d128(group, paired, qmap, kmap_tc, vmap_tc, ta,
-                                                        grid, s);
-                default: return launch_prefill_tc_d256(group, paired, qmap, kmap_tc, vmap_tc, ta,
-                                                       grid, s);
-            }
-        };
-        // requests whose rows span two or more query blocks: clusters of
-        // kTcCluster CTAs sharing every K/V tile; virtual cluster ids: request r
-        // owns cu_seqlens_q[r] / (kTcCluster bq) + r ...
-        if (max_seqlen_q > bq) {
-            const int64_t ncl = total_q / (kTcCluster * bq) + num_seqs;
-            ce = launch_tc(true, dim3((unsigned)(kTcCluster * ncl), num_kv_heads, 1));
-            if (ce != cudaSuccess) return cuda_fail(ce, "paged_prefill_tc (paired) launch");
+        // one CTA per (query block, KV head); virtual block ids: request r owns
+        // cu_seqlens_q[r] / bq + r onward
+        const int64_t nblk = total_q / bq + num_seqs;
+        const dim3 grid((unsigned)nblk, num_kv_heads, 1);
+        switch (head_dim) {
+            case 64: ce = launch_prefill_tc_d64(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
+            case 128: ce = launch_prefill_tc_d128(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
+            default: ce = launch_prefill_tc_d256(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
         }
-        // requests whose rows fit one query block (verify windows, short chunks)
-        ce = launch_tc(false, dim3((unsigned)num_seqs, num_kv_heads, 1));
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_prefill_tc launch");
     } else if (max_seqlen_q > 1) {
         a.mode = 1;

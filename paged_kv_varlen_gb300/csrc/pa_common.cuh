@@ -147,24 +147,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int x
         : "memory");
 }
 
-// Same, multicast: the box lands at the same shared-memory offset in every CTA
-// of the cluster named in `mask`, each completing on its own barrier there.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void *map, int x, int y, int z,
-                                               uint32_t bar, uint16_t mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6, %7;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask),
-        "l"(policy)
-        : "memory");
-}
-
-// All threads of every CTA in the cluster meet here (release / acquire).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-                 ::: "memory");
-}
-
 // ---------------------------------------------------------------- smem access
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;

@@ -8,6 +8,8 @@
 
 #include <utility>
 
+#include "pa.h"
+
 namespace pa {
 
 constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
@@ -94,8 +96,6 @@ struct DecodeTcArgs {
 // Keys per K/V tile of the tensor-core kernel and query rows per block.
 __host__ __device__ constexpr int tc_tile_keys(int head_dim) { return head_dim >= 256 ? 64 : 128; }
 __host__ __device__ constexpr int tc_block_rows(int group) { return 128 / group; }
-// CTAs of a cluster that share every K/V tile of a request (TMA multicast).
-constexpr int kTcCluster = 4;
 
 struct ReduceArgs {
     void *out;
@@ -170,13 +170,21 @@ __host__ __device__ constexpr int gcd_int(int a, int b) { return b == 0 ? a : gc
 // Message returned by pa_last_error_string() on this thread.
 void set_last_error(const char *msg);
 
-// Tensor-core kernel for multi-query rows, per head_dim (bf16 only).  paired:
-// clusters of kTcCluster CTAs over requests with two or more query blocks
-// (grid.x = kTcCluster * (total_q / (kTcCluster * BQ) + num_seqs)); single:
-// one CTA per request whose rows
-// fit one block (grid.x = num_seqs).  grid.y = num_kv_heads.
+// Host-side argument checks of pa_varlen_attention (no device call); sets the
+// message of pa_last_error_string() on failure.
+pa_status check_attention_args(const void *out, const void *q, const void *key_cache,
+                               const void *value_cache, const int32_t *cu_seqlens_q,
+                               const int32_t *seq_lens_k, const int32_t *block_tables,
+                               int max_blocks_per_seq, int num_seqs, int64_t total_q,
+                               int max_seqlen_q, int max_seqlen_k, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                               const float *sinks, int partition_size, pa_dtype dtype);
+
+// Tensor-core kernel for multi-query rows, per head_dim (bf16 only): one CTA
+// per (query block of BQ rows, KV head); grid.x = total_q / BQ + num_seqs
+// virtual blocks, grid.y = num_kv_heads.
 #define PA_DECLARE_TC(NAME) \
-    cudaError_t NAME(int group, bool paired, const CUtensorMap &qmap, const CUtensorMap &kmap, \
+    cudaError_t NAME(int group, const CUtensorMap &qmap, const CUtensorMap &kmap, \
                      const CUtensorMap &vmap, const TcArgs &a, dim3 grid, cudaStream_t stream);
 PA_DECLARE_TC(launch_prefill_tc_d64)
 PA_DECLARE_TC(launch_prefill_tc_d128)

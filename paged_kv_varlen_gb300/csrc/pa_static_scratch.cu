@@ -62,41 +62,19 @@ PA_API pa_status pa_varlen_attention_static_scratch(
     int num_q_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
     float scale, const float *sinks, int causal, int partition_size, pa_dtype dtype,
     void *stream) {
-    // no rows: the attention call's own checks and its PA_OK, with no device query
-    if (total_q == 0)
-        return pa_varlen_attention(out, q, key_cache, value_cache, cu_seqlens_q, seq_lens_k,
-                                   block_tables, max_blocks_per_seq, num_seqs, total_q,
-                                   max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads,
-                                   head_dim, block_size, num_blocks, scale, sinks, causal,
-                                   partition_size, nullptr, 0, dtype, stream);
-    if (total_q > 0 && num_seqs > 0 && num_q_heads > 0 && head_dim > 0 && num_kv_heads > 0) {
-        // The scratch this call's split plan needs (the plan depends on the
-        // device's SM count, read without allocating anything).
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            set_last_error("static scratch: cannot query the current device");
-            return PA_ERR_CUDA;
-        }
-        if (partition_size < -1) return PA_ERR_INVALID_ARG;
-        const int P = pa_choose_partition_size(num_seqs, num_kv_heads, max_seqlen_k,
-                                               partition_size, sms);
-        const size_t need =
-            P > 0 ? pa_varlen_attention_workspace_size(num_seqs, max_seqlen_k, num_q_heads,
-                                                       head_dim, P)
-                  : 0;
-        if (need > PA_STATIC_SCRATCH_BYTES) {
-            char msg[256];
-            snprintf(msg, sizeof msg,
-                     "static scratch: this call needs %zu bytes of split-KV scratch, more than "
-                     "the %u-byte static array; pass a workspace to pa_varlen_attention",
-                     need, (unsigned)PA_STATIC_SCRATCH_BYTES);
-            set_last_error(msg);
-            return PA_ERR_WORKSPACE;
-        }
-    }
+    // the attention call's own argument checks come first, so a bad argument
+    // gets the same status (and message) as from pa_varlen_attention
+    pa_status st = check_attention_args(out, q, key_cache, value_cache, cu_seqlens_q, seq_lens_k,
+                                        block_tables, max_blocks_per_seq, num_seqs, total_q,
+                                        max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads,
+                                        head_dim, block_size, num_blocks, sinks, partition_size,
+                                        dtype);
+    if (st != PA_OK || total_q == 0) return st;
+    // A split plan that needs more than the array holds is refused by the
+    // attention call's workspace check, before any launch, with the bytes it
+    // needed in pa_last_error_string().
     void *scratch = nullptr;
-    pa_status st = scratch_address(&scratch);
+    st = scratch_address(&scratch);
     if (st != PA_OK) return st;
     return pa_varlen_attention(out, q, key_cache, value_cache, cu_seqlens_q, seq_lens_k,
                                block_tables, max_blocks_per_seq, num_seqs, total_q, max_seqlen_q,

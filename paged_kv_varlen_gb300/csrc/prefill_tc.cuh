@@ -73,18 +73,16 @@ struct TcCfg {
     static_assert(BN % 64 == 0 && D % 64 == 0, "tile shape");
 };
 
-// PAIR: a cluster of kTcCluster CTAs takes adjacent query blocks of one
-// request and KV head; all walk the same K/V tiles and each CTA loads its
-// share of every tile's TMA boxes with multicast into all of them, dividing
-// the per-SM box issue (the gather's limit) by the cluster size.  Without
-// PAIR a CTA takes a request whose rows fit one query block.
-template <int D, int G, bool PAIR>
+// One CTA per (request, KV head, query block of BQ rows).  Virtual block p
+// belongs to the last request r with cu_seqlens_q[r] / BQ + r <= p (a
+// request of n rows owns ceil(n / BQ) <= n / BQ + 1 of them); single-row
+// requests and the padding of the numbering leave at once.
+template <int D, int G>
 __global__ void __launch_bounds__(352, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                             const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const TcArgs a) {
     using C = TcCfg<D, G>;
-    constexpr int CL = PAIR ? kTcCluster : 1;          // CTAs sharing each K/V tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -113,47 +111,32 @@ __global__ void __launch_bounds__(352, 1)
     const int bs = a.block_size;
 
     // ---------------------------------------------------------------- work item
-    int r, i0, rows, kend, rot_seed;
-    if (PAIR) {
-        // Virtual cluster p belongs to the last request r with
-        // cu[r] / (CL BQ) + r <= p; CTA `rank` of the cluster takes block CL l + rank.
-        const int p = blockIdx.x / CL;
-        const int rank = blockIdx.x % CL;
+    const int p = blockIdx.x;
+    int r;
+    {
         int lo = 0, hi = a.num_seqs - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (a.cu_seqlens_q[mid] / (CL * C::BQ) + mid <= p) lo = mid;
+            if (a.cu_seqlens_q[mid] / C::BQ + mid <= p) lo = mid;
             else hi = mid - 1;
         }
         r = lo;
+    }
+    int i0, rows, kend;
+    {
         const int c0r = a.cu_seqlens_q[r];
         const int nr = a.cu_seqlens_q[r + 1] - c0r;
         const int nblk = (nr + C::BQ - 1) / C::BQ;
-        const int ngroups = (nblk + CL - 1) / CL;
-        const int lp = p - (c0r / (CL * C::BQ) + r);
-        if (nblk < 2 || lp < 0 || lp >= ngroups) return;  // whole cluster leaves together
-        const int lpp = ngroups - 1 - lp;                   // heaviest cluster first
-        const int qb = CL * lpp + rank;                     // may be past the last block
-        const int qb_hi = min(CL * lpp + CL - 1, nblk - 1);   // the cluster's heaviest block
+        const int lp = p - (c0r / C::BQ + r);
+        if (nr <= 1 || lp < 0 || lp >= nblk) return;
+        const int qb = nblk - 1 - lp;                       // heaviest (last) block first
         i0 = qb * C::BQ;
-        rows = qb < nblk ? min(C::BQ, nr - i0) : 0;
+        rows = min(C::BQ, nr - i0);
         int Nr = a.seq_lens_k[r];
         Nr = max(0, min(Nr, a.max_blocks_per_seq * bs));
-        const int i0_hi = qb_hi * C::BQ;
-        const int rows_hi = min(C::BQ, nr - i0_hi);
-        kend = max(0, a.causal ? min(Nr, Nr - nr + i0_hi + rows_hi) : Nr);
-        rot_seed = p;
-    } else {
-        r = blockIdx.x;
-        const int nr = a.cu_seqlens_q[r + 1] - a.cu_seqlens_q[r];
-        if (nr <= 1 || nr > C::BQ) return;                 // decode rows / paired launch
-        int Nr = a.seq_lens_k[r];
-        Nr = max(0, min(Nr, a.max_blocks_per_seq * bs));
-        i0 = 0;
-        rows = nr;
-        kend = max(0, a.causal ? min(Nr, Nr - nr + rows) : Nr);
-        rot_seed = blockIdx.x;
+        kend = max(0, a.causal ? min(Nr, Nr - nr + i0 + rows) : Nr);
     }
+    const int rot_seed = p;
     const int c0 = a.cu_seqlens_q[r];
     const int n = a.cu_seqlens_q[r + 1] - c0;
     int N = a.seq_lens_k[r];
@@ -162,24 +145,22 @@ __global__ void __launch_bounds__(352, 1)
     const int64_t row_base = (int64_t)c0 + i0;
     // The blocks of one request read the same keys: each starts at its own tile
     // and wraps around, so they do not all hit the same L2 lines at once (the
-    // online softmax does not depend on the order of the tiles).  Both CTAs of a
-    // pair use the same order.
+    // online softmax does not depend on the order of the tiles).
     const int rot = ntiles > 1
         ? (int)(((uint32_t)rot_seed * 2654435761u + (uint32_t)blockIdx.y * 40503u) % ntiles)
         : 0;
     auto tile_of = [&](int j) { const int jt = j + rot; return jt >= ntiles ? jt - ntiles : jt; };
-    constexpr uint16_t kPairMask = (uint16_t)((1u << CL) - 1);   // every CTA of the cluster
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
         mbar_init(bar_q, 1);
         for (int s = 0; s < C::NK; ++s) {
             mbar_init(bar_k_full + 8 * s, 1);
-            mbar_init(bar_k_empty + 8 * s, CL);   // every CTA of the cluster releases a stage
+            mbar_init(bar_k_empty + 8 * s, 1);
         }
         for (int s = 0; s < C::NV; ++s) {
             mbar_init(bar_v_full + 8 * s, 1);
-            mbar_init(bar_v_empty + 8 * s, CL);
+            mbar_init(bar_v_empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_s_full + 8 * b, 1);
@@ -206,7 +187,6 @@ __global__ void __launch_bounds__(352, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -266,24 +246,15 @@ __global__ void __launch_bounds__(352, 1)
             if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * st, nsub * C::KCH * BR * 128);
             __syncwarp();
             const uint32_t dst = stage0 + st * C::KV_TILE;
-            // cluster: CTA rk loads boxes [rk nsub / CL, (rk + 1) nsub / CL), each
-            // multicast to every CTA (every CTA expects the whole tile)
-            const int rk = (int)(blockIdx.x % CL);
-            const int u_lo = rk * nsub / CL;
-            const int u_hi = (rk + 1) * nsub / CL;
-            if (lane == 0) {
-                for (int u = u_lo; u < u_hi; ++u) {
-                    const int row0 = pgt[u] * bs + (kt + u * BR) % bs;
+            // the tile's boxes are spread over the warp's lanes (lane u issues the
+            // boxes of page run u), so several TMA issues are in flight at once
+            if (lane < nsub) {
+                const int u = lane;
+                const int row0 = pgt[u] * bs + (kt + u * BR) % bs;
 #pragma unroll
-                    for (int c = 0; c < C::KCH; ++c) {
-                        const uint32_t d = dst + c * C::BN * 128 + u * BR * 128;
-                        if (PAIR)
-                            tma_load_3d_mc(d, map, c * 64, h, row0, bar_full + 8 * st,
-                                           kPairMask, pol_kv);
-                        else
-                            tma_load_3d(d, map, c * 64, h, row0, bar_full + 8 * st, pol_kv);
-                    }
-                }
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_3d(dst + c * C::BN * 128 + u * BR * 128, map, c * 64, h, row0,
+                                bar_full + 8 * st, pol_kv);
             }
             __syncwarp();
             issued = j + 1;
@@ -318,8 +289,7 @@ __global__ void __launch_bounds__(352, 1)
                                    (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar_o_done + 8 * pb);
-                if (PAIR) tc_commit_mc(bar_v_empty + 8 * stp, kPairMask);
-                else tc_commit(bar_v_empty + 8 * stp);
+                tc_commit(bar_v_empty + 8 * stp);
             };
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j % C::NK;
@@ -338,8 +308,7 @@ __global__ void __launch_bounds__(352, 1)
                     tc_mma_bf16(tmem + sb * C::BN, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bar_s_full + 8 * sb);
-                if (PAIR) tc_commit_mc(bar_k_empty + 8 * st, kPairMask);
-                else tc_commit(bar_k_empty + 8 * st);
+                tc_commit(bar_k_empty + 8 * st);
                 if (j >= 1) issue_pv(j - 1);
             }
             issue_pv(ntiles - 1);
@@ -541,60 +510,38 @@ __global__ void __launch_bounds__(352, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    // no CTA of a pair leaves while its peer may still multicast into it or
-    // arrive on its barriers
-    if (PAIR) cluster_sync();
 }
 
-template <int D, int G, bool PAIR>
+template <int D, int G>
 cudaError_t launch_prefill_tc_t(const CUtensorMap &qmap, const CUtensorMap &kmap,
                                 const CUtensorMap &vmap, const TcArgs &a, dim3 grid,
                                 cudaStream_t stream) {
     using C = TcCfg<D, G>;
-    auto kern = paged_prefill_tc_kernel<D, G, PAIR>;
+    auto kern = paged_prefill_tc_kernel<D, G>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        if (PAIR) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-            if (e != cudaSuccess) return e;
-        }
         configured = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    if (PAIR) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = kTcCluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, a);
-    if (e != cudaSuccess) return e;
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(qmap, kmap, vmap, a);
     return cudaGetLastError();
 }
 
-template <int D, bool PAIR>
+template <int D>
 cudaError_t launch_prefill_tc_group(int group, const CUtensorMap &qmap, const CUtensorMap &kmap,
                                     const CUtensorMap &vmap, const TcArgs &a, dim3 grid,
                                     cudaStream_t stream) {
     switch (group) {
-        case 1: return launch_prefill_tc_t<D, 1, PAIR>(qmap, kmap, vmap, a, grid, stream);
-        case 2: return launch_prefill_tc_t<D, 2, PAIR>(qmap, kmap, vmap, a, grid, stream);
-        case 3: return launch_prefill_tc_t<D, 3, PAIR>(qmap, kmap, vmap, a, grid, stream);
-        case 4: return launch_prefill_tc_t<D, 4, PAIR>(qmap, kmap, vmap, a, grid, stream);
-        case 5: return launch_prefill_tc_t<D, 5, PAIR>(qmap, kmap, vmap, a, grid, stream);
-        case 6: return launch_prefill_tc_t<D, 6, PAIR>(qmap, kmap, vmap, a, grid, stream);
-        case 7: return launch_prefill_tc_t<D, 7, PAIR>(qmap, kmap, vmap, a, grid, stream);
-        case 8: return launch_prefill_tc_t<D, 8, PAIR>(qmap, kmap, vmap, a, grid, stream);
+        case 1: return launch_prefill_tc_t<D, 1>(qmap, kmap, vmap, a, grid, stream);
+        case 2: return launch_prefill_tc_t<D, 2>(qmap, kmap, vmap, a, grid, stream);
+        case 3: return launch_prefill_tc_t<D, 3>(qmap, kmap, vmap, a, grid, stream);
+        case 4: return launch_prefill_tc_t<D, 4>(qmap, kmap, vmap, a, grid, stream);
+        case 5: return launch_prefill_tc_t<D, 5>(qmap, kmap, vmap, a, grid, stream);
+        case 6: return launch_prefill_tc_t<D, 6>(qmap, kmap, vmap, a, grid, stream);
+        case 7: return launch_prefill_tc_t<D, 7>(qmap, kmap, vmap, a, grid, stream);
+        case 8: return launch_prefill_tc_t<D, 8>(qmap, kmap, vmap, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

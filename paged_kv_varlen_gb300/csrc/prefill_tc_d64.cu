@@ -1,14 +1,13 @@
 // Instantiations of the tensor-core multi-query-row kernel for head_dim 64
-// (query-head groups 1..8, paired and single CTAs); see prefill_tc.cuh.
+// (query-head groups 1..8); see prefill_tc.cuh.
 #include "prefill_tc.cuh"
 
 namespace pa {
 
-cudaError_t launch_prefill_tc_d64(int group, bool paired, const CUtensorMap &qmap,
-                                  const CUtensorMap &kmap, const CUtensorMap &vmap,
-                                  const TcArgs &a, dim3 grid, cudaStream_t stream) {
-    return paired ? launch_prefill_tc_group<64, true>(group, qmap, kmap, vmap, a, grid, stream)
-                  : launch_prefill_tc_group<64, false>(group, qmap, kmap, vmap, a, grid, stream);
+cudaError_t launch_prefill_tc_d64(int group, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                                  const CUtensorMap &vmap, const TcArgs &a, dim3 grid,
+                                  cudaStream_t stream) {
+    return launch_prefill_tc_group<64>(group, qmap, kmap, vmap, a, grid, stream);
 }
 
 }  // namespace pa

@@ -87,15 +87,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
         : "memory");
 }
 
-// Same, arriving on the barrier at this offset in every CTA named in `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-}
-
 // ---------------------------------------------------------------- TMEM <-> registers
 // 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
 // 32w .. 32w + 31 of the address's lane field).

@@ -113,20 +113,50 @@ def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
     return mx, mean
 
 
-def check_step(w: wl.Workload, rows=None, partition_size=None, nthreads=None):
-    """Scatter + attention on the GPU vs the oracle (bit-exact cache, tolerance
-    on the sampled output rows).  Returns (max err, mean err)."""
-    dw = DeviceWorkload(w)
-    dw.scatter()
+def check_scatter(dw: "DeviceWorkload", slot_mapping=None):
+    """Runs the GPU scatter and checks the WHOLE pool: the pages this step
+    touches bit for bit against the oracle's scatter, every other page bit for
+    bit against its bytes before the step (compared on the device, so a large
+    pool costs no host copy).  Slots past the pool are skipped like negative
+    ones (reading R5), so the oracle gets -1 for them.  Returns the oracle's
+    pools."""
+    w = dw.w
+    sm = w.slot_mapping if slot_mapping is None else np.asarray(slot_mapping, np.int64)
+    nslots = w.num_blocks * w.block_size
+    kc_before = dev_bits_t(dw.key_cache).clone()
+    vc_before = dev_bits_t(dw.value_cache).clone()
+    pa.pa_reshape_and_cache(dw.new_k, dw.new_v, dw.key_cache, dw.value_cache,
+                            torch.from_numpy(sm).to(dw.key_cache.device))
+    sm_oracle = np.where((sm >= 0) & (sm < nslots), sm, -1)
     kc_ref, vc_ref = orc.reshape_and_cache(w.new_k, w.new_v, w.key_cache, w.value_cache,
-                                           w.slot_mapping, w.block_size)
-    # bit-exact scatter (compare only the pages the step touched, plus a sample)
-    pages = np.unique(w.slot_mapping[w.slot_mapping >= 0] // w.block_size)
-    got_k = dev_bits(dw.key_cache[torch.from_numpy(pages).cuda()])
-    got_v = dev_bits(dw.value_cache[torch.from_numpy(pages).cuda()])
+                                           sm_oracle, w.block_size)
+    pages = np.unique(sm_oracle[sm_oracle >= 0] // w.block_size)
     view = np.uint16 if w.dtype == wl.BF16 else np.uint32
-    assert np.array_equal(got_k, kc_ref[pages].view(view)), "key cache scatter differs"
-    assert np.array_equal(got_v, vc_ref[pages].view(view)), "value cache scatter differs"
+    pidx = torch.from_numpy(pages).to(dw.key_cache.device)
+    assert np.array_equal(dev_bits(dw.key_cache[pidx]), kc_ref[pages].view(view)), \
+        "key cache scatter differs"
+    assert np.array_equal(dev_bits(dw.value_cache[pidx]), vc_ref[pages].view(view)), \
+        "value cache scatter differs"
+    untouched = torch.ones(w.num_blocks, dtype=torch.bool, device=dw.key_cache.device)
+    untouched[pidx] = False
+    assert torch.equal(dev_bits_t(dw.key_cache)[untouched], kc_before[untouched]), \
+        "the scatter wrote a page no token maps to (key cache)"
+    assert torch.equal(dev_bits_t(dw.value_cache)[untouched], vc_before[untouched]), \
+        "the scatter wrote a page no token maps to (value cache)"
+    return kc_ref, vc_ref
+
+
+def dev_bits_t(t: torch.Tensor) -> torch.Tensor:
+    """Bit view of a device tensor (NaN payloads compare equal)."""
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+def check_step(w: wl.Workload, rows=None, partition_size=None, nthreads=None):
+    """Scatter + attention on the GPU vs the oracle (bit-exact whole pool after
+    the scatter, tolerance on the sampled output rows).  Returns (max err,
+    mean err)."""
+    dw = DeviceWorkload(w)
+    kc_ref, vc_ref = check_scatter(dw)
     dw.attention(partition_size=partition_size)
     torch.cuda.synchronize()
     assert pa.pa_device_error() == 0

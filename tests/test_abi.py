@@ -149,6 +149,42 @@ def test_static_scratch_with_no_rows_needs_no_device(lib):
     assert f(*base, 7, None) == 1
 
 
+@pytest.mark.parametrize("over,status", [
+    (dict(dtype=7), 1),               # unknown dtype
+    (dict(out=0), 1),                 # null output
+    (dict(q=24), 1),                  # misaligned query pointer
+    (dict(P=100), 1),                 # partition not a multiple of 32
+    (dict(P=-5), 1),                  # partition below -1
+    (dict(D=96), 2),                  # head_dim not compiled
+    (dict(Hq=72, Hkv=8), 2),          # group of 9 > 8
+])
+def test_static_scratch_checks_arguments_like_the_workspace_call(lib, over, status):
+    """A bad argument gets the same status and message from the allocation-free
+    call as from pa_varlen_attention, even when the split plan would need far
+    more than the static array (64 requests of 64k keys), and before any device
+    query (these run without a GPU)."""
+    v = ctypes.c_void_p
+    f = lib.pa_varlen_attention_static_scratch
+    f.restype = ctypes.c_int
+    f.argtypes = [v, v, v, v, v, v, v, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int64, ctypes.c_float, v, ctypes.c_int, ctypes.c_int, ctypes.c_int, v]
+    a = dict(out=16, q=16, kc=16, vc=16, cu=16, sl=16, bt=16, mbps=4096, S=64, total_q=64,
+             mq=1, mk=65536, Hq=32, Hkv=8, D=128, bs=16, nb=4096, scale=0.1, sinks=None,
+             causal=1, P=256, dtype=1)
+    a.update(over)
+    got = f(v(a["out"]), v(a["q"]), v(a["kc"]), v(a["vc"]), v(a["cu"]), v(a["sl"]), v(a["bt"]),
+            a["mbps"], a["S"], a["total_q"], a["mq"], a["mk"], a["Hq"], a["Hkv"], a["D"], a["bs"],
+            a["nb"], a["scale"], a["sinks"], a["causal"], a["P"], a["dtype"], None)
+    msg = lib.pa_last_error_string().decode()
+    assert got == status
+    ref = _call_attention(lib, out=a["out"], q=a["q"], mbps=a["mbps"], S=a["S"],
+                          total_q=a["total_q"], mk=a["mk"], Hq=a["Hq"], Hkv=a["Hkv"], D=a["D"],
+                          nb=a["nb"], P=a["P"], dtype=a["dtype"])
+    assert ref == status
+    assert lib.pa_last_error_string().decode() == msg and msg != "no error"
+
+
 def test_scatter_argument_checks(lib):
     v = ctypes.c_void_p
     f = lib.pa_reshape_and_cache

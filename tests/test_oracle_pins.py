@@ -380,6 +380,48 @@ def test_scatter_is_byte_exact_and_keeps_untouched_slots():
                           w.key_cache[s1 // bs, s1 % bs].view(np.uint16))
 
 
+SCATTER_PIN_CASES = [
+    # prompt-only: every key of every request reaches the pool through the scatter
+    dict(seed=41, dtype=wl.BF16, head_dim=64, num_q_heads=4, num_kv_heads=2, block_size=16,
+         num_seqs=4, prior=0, max_q=40),
+    dict(seed=42, dtype=wl.F32, head_dim=32, num_q_heads=6, num_kv_heads=3, block_size=8,
+         num_seqs=3, prior=0, max_q=30),
+    # prior context already in the pool, this step's tokens through the scatter
+    dict(seed=43, dtype=wl.BF16, head_dim=64, num_q_heads=8, num_kv_heads=1, block_size=32,
+         num_seqs=5, prior=90, max_q=12),
+]
+
+
+@pytest.mark.parametrize("case", SCATTER_PIN_CASES, ids=lambda c: f"seed{c['seed']}")
+def test_scatter_then_attention_equals_dense_bruteforce(case):
+    """The oracle's scatter pinned by what attention reads back: a poisoned pool
+    (every slot NaN) receives this step's K/V rows only through
+    oracle.reshape_and_cache; oracle attention over it must equal dense
+    attention on the unpaged per-request K/V.  A row scattered to the wrong page
+    or slot, or a token dropped, leaves a NaN or a wrong key where attention
+    reads, so the pin fails (kwkr.cn kernel table: reshape_and_cache writes the
+    rows attention then gathers through the block table)."""
+    c = dict(case)
+    prior_max, max_q = c.pop("prior"), c.pop("max_q")
+    rng = np.random.default_rng(c["seed"])
+    S = c.pop("num_seqs")
+    prior = rng.integers(0, prior_max, size=S, endpoint=True) if prior_max else np.zeros(S, int)
+    q = rng.integers(1, max_q, size=S, endpoint=True)
+    seed = c.pop("seed")
+    w = wl.build(f"scatter_pin_{seed}", c.pop("dtype"), c.pop("num_q_heads"),
+                 c.pop("num_kv_heads"), c.pop("head_dim"), c.pop("block_size"), prior, q,
+                 seed=seed, pool_slack=1.5, poison=True)
+    assert not c
+    kc, vc = oracle.reshape_and_cache(w.new_k, w.new_v, w.key_cache, w.value_cache,
+                                      w.slot_mapping, w.block_size)
+    got = attention_of(w, key_cache=kc, value_cache=vc)
+    assert np.isfinite(got).all()
+    assert np.max(np.abs(got - dense_bruteforce(w))) < 1e-12
+    # without the scatter the poisoned slots reach attention: the pin can fail
+    bad = attention_of(w, key_cache=w.key_cache, value_cache=w.value_cache)
+    assert not np.isfinite(bad).all()
+
+
 def test_scatter_rejects_slot_outside_pool():
     w = wl.random_small(24, dtype=wl.F32)
     sm = w.slot_mapping.copy(); sm[0] = w.num_blocks * w.block_size

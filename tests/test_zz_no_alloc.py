@@ -36,13 +36,22 @@ def test_static_scratch_matches_workspace_call_twice(dtype):
                         head_dim=128, block_size=16, max_prior=3000, max_q=3, with_sinks=True)
     w2 = wl.random_small(4243, dtype=dtype, num_seqs=5, num_q_heads=8, num_kv_heads=2,
                          head_dim=128, block_size=16, max_prior=1800, max_q=1)
-    for case in (w, w2):                     # two calls in a row, different shapes
+    for i, case in enumerate((w, w2)):       # two calls in a row, different shapes
         dw = DeviceWorkload(case)
         dw.scatter()
         ref = dw.attention(partition_size=256, out=torch.empty_like(dw.q))
         out = torch.full_like(dw.q, float("nan"))
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
+        torch_before = torch.cuda.memory_allocated()
         _static_call(dw, out, 256)
         torch.cuda.synchronize()
+        if i == 1:
+            # after the first call has looked up the array's address (which may
+            # load the library's module holding it), a call changes neither the
+            # device's free memory nor torch's allocations
+            assert torch.cuda.mem_get_info()[0] == free_before
+            assert torch.cuda.memory_allocated() == torch_before
         assert_close(from_dev(out), from_dev(ref), case.dtype, f"static scratch {case.name}")
         assert pa.pa_device_error() == 0
 
@@ -56,7 +65,7 @@ def test_static_scratch_refuses_calls_that_need_more():
     sl = torch.full((64,), 16, dtype=torch.int32, device="cuda")
     bt = torch.zeros(64, 4096, dtype=torch.int32, device="cuda")
     out = torch.zeros_like(q)
-    with pytest.raises(pa.PAError, match="WORKSPACE"):
+    with pytest.raises(pa.PAError, match="WORKSPACE.*needs [0-9]+ bytes"):
         pa.pa_varlen_attention_static_scratch(out, q, kc, kc, cu, sl, bt, max_seqlen_q=1,
                                               max_seqlen_k=65536, scale=0.1,
                                               partition_size=256)
