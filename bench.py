@@ -6,12 +6,14 @@ this step's tokens, then attention over the packed query rows and paged K/V
 tcgen05 kernel for multi-query rows) -- one pa_scatter_and_attend call
 (``--step two-call``: pa_reshape_and_cache then pa_varlen_attention).
 
-Default workload (the one the headline metric is quoted on): the GQA decode
-batch -- 32 requests with contexts U[512, 8192], (H_q, H_kv, D) = (32, 8, 128),
-bf16, block size 16, 40k-page shuffled pool, split-KV partition 512.  Metric:
-decode KV GB/s = algorithmic bytes per step / step time.  ``--workload`` picks
-another seeded workload (2: varlen causal prefill -> TFLOP/s; 3: mixed packed
-step -> tokens/s; 4: long-context decode with sinks -> GB/s).
+Headline workload (``value``): the GQA decode batch -- 32 requests with
+contexts U[512, 8192], (H_q, H_kv, D) = (32, 8, 128), bf16, block size 16,
+40k-page shuffled pool, split-KV partition 512.  Metric: decode KV GB/s =
+algorithmic bytes per step / step time.  The default run also times the other
+three workloads of the metric, each in a sub-record of the same JSON line
+(``workloads``: 2 varlen causal prefill -> TFLOP/s; 3 mixed packed step ->
+tokens/s; 4 long-context decode with sinks -> GB/s), each with its own
+roofline, end-to-end figure and CPU baseline.  ``--workload N`` times only N.
 
 Algorithmic work per step: every visible (query row, key) pair costs
 4 * D flops per query head (QK^T and PV); bytes are each context token's K and
@@ -21,7 +23,7 @@ workloads, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload 1..4] [--no-cpu-baseline] [--layout packed|padded]
-                    [--step two-call|fused]
+                    [--step two-call|fused] [--only-primary]
 
 Under torchrun (N > 1) every rank runs its own independent batch (requests are
 independent units: weak scaling, no collective on the data path); timing is
@@ -51,13 +53,13 @@ DEFAULT_WORKLOAD = 1
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum per attention call from an ncu
-# capture, valid only for the kernel sources whose hash is recorded beside it.
-# DRAM bytes (read + write) of one paged_decode_tc_kernel launch on workload 1,
-# from ncu (dram__bytes_read.sum + dram__bytes_write.sum); valid while the
-# kernel sources hash to the value below.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one
+# paged_decode_tc_kernel launch on workload 1, from an ncu capture of the
+# kernel sources whose hash is recorded beside it; reported as null once the
+# sources change, until a new capture is taken.
 NCU_TRAFFIC = {"sources_sha256": "762a3d5dd94725543cbd07b956d98f6bd4e443cec73bf4cf281bb576196db805",
-               "bytes_per_launch": 526379776 + 5281536, "workload": 1}
+               "bytes_per_launch": 526379776 + 5281536, "workload": 1,
+               "kernel": "paged_decode_tc_kernel"}
 
 
 def kernel_sources_hash() -> str:
@@ -247,28 +249,51 @@ def sample_rows(w, target_flops: float, seed: int = 0):
     return np.sort(rng.choice(w.total_q, size=k, replace=False))
 
 
-def cpu_baseline(w, kind, budget_s=12.0):
-    """The oracle as it stands on all host cores, on samples of the workload's
-    rows until about `budget_s` of CPU work."""
+def cpu_baseline(w, kind, budget_s=8.0, budget_1core_s=4.0):
+    """The oracle as it stands, on samples of the workload's rows: on all host
+    cores until about `budget_s` of wall time, and on one core until about
+    `budget_1core_s`."""
     nthreads = os.cpu_count() or 1
     prepare_oracle_pool(w)
-    rows = sample_rows(w, 4e9)
-    t, n = 0.0, 0
-    while t < budget_s and n < 1000:
-        t += time_oracle(w, rows, nthreads)
-        n += 1
-    work = {k: v * n for k, v in rows_work(w, rows).items()}
-    value, unit = metric_value(kind, work, t, 1)
+
+    def timed(target_flops, threads, budget):
+        rows = sample_rows(w, target_flops)
+        t, n = 0.0, 0
+        while t < budget and n < 1000:
+            t += time_oracle(w, rows, threads)
+            n += 1
+        work = {k: v * n for k, v in rows_work(w, rows).items()}
+        value, unit = metric_value(kind, work, t, 1)
+        return value, unit, (f"{n} pass(es) over {len(rows)} of {w.total_q} query rows "
+                             f"(all heads), fp64 C oracle, {t:.1f} s wall")
+
+    value, unit, sample = timed(4e9, nthreads, budget_s)
+    v1, _, sample1 = timed(4e9 / max(1, nthreads), 1, budget_1core_s)
     return {"value": round(value, 6), "unit": unit, "cores": nthreads, "kind": "oracle",
-            "sample": f"{n} pass(es) over {len(rows)} of {w.total_q} query rows (all heads), "
-                      f"fp64 C oracle, {t:.1f} s wall"}
+            "sample": sample,
+            "single_core": {"value": round(v1, 6), "unit": unit, "cores": 1, "sample": sample1}}
+
+
+def workload_config(w, widx, P_used, layout, step, world, work):
+    return {"workload": WORKLOAD_NAMES_CACHE[widx], "num_seqs": w.num_seqs,
+            "total_q": w.total_q, "total_kv_tokens": int(w.seq_lens.sum()),
+            "partition_size": P_used,
+            "l2": "no flush: the KV read per step exceeds the 126 MB L2"
+                  if work["kv"] > 2 * 126e6 else "no flush (KV partly L2-resident)",
+            "parallelism": f"independent batch per GPU x{world}",
+            "layout": layout, "step": step}
+
+
+WORKLOAD_NAMES_CACHE = {}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
     from paged_kv_varlen_gb300 import workloads as wl
-    w = wl.workload(args.workload)
+    WORKLOAD_NAMES_CACHE.update(wl.WORKLOAD_NAMES)
+    widx = args.workload or DEFAULT_WORKLOAD
+    w = wl.workload(widx)
     kind = workload_kind(w)
     prepare_oracle_pool(w)
     nthreads = os.cpu_count() or 1
@@ -286,12 +311,17 @@ def run_reference(args, rank, world):
             work[k] += v
     value, unit = metric_value(kind, work, t_total, 1)
     sample = "one query row (all heads) per step, cycling over the batch; fp64 C oracle"
+    P_used = w.partition_size
+    fused = args.step == "fused"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * t_total / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.WORKLOAD_NAMES[args.workload], "sample": sample},
+        "config": workload_config(w, widx, P_used, args.layout,
+                                  "pa_scatter_and_attend" if fused
+                                  else "pa_reshape_and_cache + pa_varlen_attention", world,
+                                  algorithmic_work(w)),
         "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": nthreads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
@@ -302,18 +332,16 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ GPU arm
-def run_ours(args, rank, world, local):
+def measure(args, widx, rank, world, local, with_cpu_baseline):
+    """Times one workload on this rank's GPU: the device-resident step, the
+    end-to-end step through host buffers, the roofline of the attention call.
+    Returns the record (the JSON line's fields)."""
     import torch
     from paged_kv_varlen_gb300 import binding as pa
     from paged_kv_varlen_gb300 import workloads as wl
 
-    torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
-
-    w = wl.workload(args.workload)
+    w = wl.workload(widx)
     kind = workload_kind(w)
     work = algorithmic_work(w)
     w_useful = w
@@ -446,7 +474,7 @@ def run_ours(args, rank, world, local):
     t_fl = work["flops"] / (bf16 * 1e12)
     traffic = (NCU_TRAFFIC["bytes_per_launch"]
                if NCU_TRAFFIC["sources_sha256"] == kernel_sources_hash()
-               and NCU_TRAFFIC.get("workload") == args.workload else None)
+               and NCU_TRAFFIC.get("workload") == widx else None)
     if kind == "decode" or (kind == "mixed" and t_bw >= t_fl):
         roof = {"bound": "hbm", "achieved": round(call_bytes / attn_avg_s / 1e9, 2),
                 "peak": hbm, "unit": "GB/s"}
@@ -455,6 +483,8 @@ def run_ours(args, rank, world, local):
                 "peak": bf16, "unit": "TFLOP/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = traffic
+    if traffic is not None:
+        roof["traffic_kernel"] = NCU_TRAFFIC["kernel"]
     dec = "paged_decode_tc_kernel" if tc_decode else "paged_decode_kernel"
     if fused:
         dec = "scatter_rows_kernel + " + dec
@@ -468,23 +498,21 @@ def run_ours(args, rank, world, local):
                            if peak_kind == "measured" else "fallback")
     roof["avg_launch_us"] = round(attn_avg_s * 1e6, 3)
     if kind == "mixed":
+        # the step needs both HBM (decode and verify rows) and the tensor cores
+        # (prefill chunks): its roofline time is the larger of the two
         roof["roofline_time_us"] = round(1e6 * max(t_bw, t_fl), 2)
+        roof["t_bw_us"] = round(1e6 * t_bw, 2)
+        roof["t_flop_us"] = round(1e6 * t_fl, 2)
         roof["frac_of_max_roofline"] = round(max(t_bw, t_fl) / attn_avg_s, 4)
 
-    line = {
+    rec = {
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(1e3 * step_s, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) Q/K/V)",
-        "config": {"workload": wl.WORKLOAD_NAMES[args.workload], "num_seqs": w.num_seqs,
-                   "total_q": w.total_q, "total_kv_tokens": int(w.seq_lens.sum()),
-                   "partition_size": P_used,
-                   "l2": "no flush: the KV read per step exceeds the 126 MB L2"
-                         if work["kv"] > 2 * 126e6 else "no flush (KV partly L2-resident)",
-                   "parallelism": f"independent batch per GPU x{world}",
-                   "layout": args.layout,
-                   "step": ("pa_scatter_and_attend" if fused
-                            else "pa_reshape_and_cache + pa_varlen_attention")},
+        "config": workload_config(w_useful, widx, P_used, args.layout,
+                                  "pa_scatter_and_attend" if fused
+                                  else "pa_reshape_and_cache + pa_varlen_attention", world, work),
         "kv_gbs": round(world * work["step_bytes"] / step_s / 1e9, 2),
         "tflops": round(world * work["flops"] / step_s / 1e12, 3),
         "tokens_per_s": round(world * w_useful.total_q / step_s, 1),
@@ -494,8 +522,36 @@ def run_ours(args, rank, world, local):
         "gpu_launches": int(launches_per_step * steps),
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w_useful, kind)
+    if rank == 0 and world == 1 and with_cpu_baseline:
+        rec["cpu_baseline"] = cpu_baseline(w_useful, kind)
+    del q, kc, vc, nk, nv, out, ws, stage
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from paged_kv_varlen_gb300 import workloads as wl
+
+    WORKLOAD_NAMES_CACHE.update(wl.WORKLOAD_NAMES)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    primary = args.workload or DEFAULT_WORKLOAD
+    with_cpu = not args.no_cpu_baseline
+    line = measure(args, primary, rank, world, local, with_cpu)
+    if args.workload is None and not args.only_primary:
+        subs = {}
+        for widx in (2, 3, 4):
+            rec = measure(args, widx, rank, world, local, with_cpu)
+            keep = ("value", "unit", "ms_per_step", "dtype", "config", "kv_gbs", "tflops",
+                    "tokens_per_s", "roofline", "e2e", "gpu_launches", "clocks",
+                    "cpu_baseline")
+            subs[str(widx)] = {k: rec[k] for k in keep if k in rec}
+        line["workloads"] = subs
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -510,7 +566,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, choices=[1, 2, 3, 4], default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", type=int, choices=[1, 2, 3, 4], default=None,
+                    help="time only this workload (default: 1 as the headline, plus 2-4 "
+                         "as sub-records)")
+    ap.add_argument("--only-primary", action="store_true",
+                    help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layout", choices=["packed", "padded"], default="packed",
                     help="padded: the same batch padded to [B, T_max] (useful work counted)")

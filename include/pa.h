@@ -259,6 +259,20 @@ pa_status pa_varlen_attention_static_scratch(
  */
 pa_status pa_device_error(int *code);
 
+/*
+ * pa_test_expire_next_wait -- test hook of the failure path; not for
+ * production use.  (The pages have no counterpart: it exists so that a test
+ * can watch a bounded wait run out.)  The next attention call of this process
+ * that launches the multi-query (tensor-core) kernel makes each of its CTAs
+ * skip the K loads of its first key tile.  The MMA warp's bounded wait for
+ * that tile gives up after about one second of GPU time; the kernel then sets
+ * the device error word, lets every other wait return at once, drains its
+ * copies and tensor-core work in flight and returns, without a trap or fault.
+ * Its output is unreliable; pa_device_error() reports a nonzero code, and the
+ * calls after it run normally.
+ */
+void pa_test_expire_next_wait(void);
+
 #ifdef __cplusplus
 }
 #endif

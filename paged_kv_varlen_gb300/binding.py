@@ -61,6 +61,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pa_split_kv_reduce.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P]
     lib.pa_device_error.restype = I
     lib.pa_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.pa_test_expire_next_wait.restype = None
+    lib.pa_test_expire_next_wait.argtypes = []
     _lib = lib
     return lib
 
@@ -219,6 +221,12 @@ def pa_device_error() -> int:
     code = ctypes.c_int(0)
     _check(load_library().pa_device_error(ctypes.byref(code)), "pa_device_error")
     return code.value
+
+
+def pa_test_expire_next_wait() -> None:
+    """Test hook: the next multi-query launch skips one K tile per CTA, so a
+    bounded wait runs out and sets the device error word (no fault)."""
+    load_library().pa_test_expire_next_wait()
 
 
 def pa_varlen_attention_static_scratch(out: torch.Tensor, q: torch.Tensor,

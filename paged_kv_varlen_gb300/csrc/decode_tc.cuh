@@ -541,43 +541,43 @@ __global__ void __launch_bounds__(224, 1)
             cp_async_wait<C::PGR - 1>();   // tile t's page ids have landed
             __syncwarp();
             int bad = 0;
-            if (lane == 0) {
-                if (is_k && j == 0) {   // Q^T of the item, rows = its G heads
-                    const int qb = itn & 1;
-                    if (itn >= 2)
-                        bad = !mbar_wait(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1, a.err,
-                                         abort_flag);
-                    if (!bad) {
-                        mbar_arrive_expect_tx(bar_q_full + 8 * qb, C::KCH * G * 128);
+            if (lane == 0 && is_k && j == 0) {   // Q^T of the item, rows = its G heads
+                const int qb = itn & 1;
+                if (itn >= 2)
+                    bad = !mbar_wait(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1, a.err,
+                                     abort_flag);
+                if (!bad) {
+                    mbar_arrive_expect_tx(bar_q_full + 8 * qb, C::KCH * G * 128);
 #pragma unroll
-                        for (int c = 0; c < C::KCH; ++c)
-                            tma_load_3d(q_smem + qb * C::Q_BUF + c * C::NP * 128, &qmap, c * 64,
-                                        cur.h * G, (int)cur.row, bar_q_full + 8 * qb, pol);
-                        q_last[0] = q_last[1];
-                        q_last[1] = itn;
-                    }
+                    for (int c = 0; c < C::KCH; ++c)
+                        tma_load_3d(q_smem + qb * C::Q_BUF + c * C::NP * 128, &qmap, c * 64,
+                                    cur.h * G, (int)cur.row, bar_q_full + 8 * qb, pol);
+                    q_last[0] = q_last[1];
+                    q_last[1] = itn;
                 }
-                const int kt = cur.k0 + j * C::BN;
-                const int nbox = (min(C::BN, cur.k1 - kt) + BR - 1) / BR;
-                const int *pgt = pgr + (t % C::PGR) * 16;
-                for (int c = 0; c < C::KS && !bad; ++c) {   // the tile's 128-dim chunks
-                    const int idx = t * C::KS + c;
-                    const int slot = idx % C::NR;
+            }
+            const int kt = cur.k0 + j * C::BN;
+            const int nbox = (min(C::BN, cur.k1 - kt) + BR - 1) / BR;
+            const int *pgt = pgr + (t % C::PGR) * 16;
+            // lane 2u + hf issues the box of page run u, 64-dim half hf: a box
+            // issue holds its warp for ~120 ns, so one box per lane keeps up to
+            // 32 issues in flight (lane 0 alone: ~16 GB/s per warp)
+            const int u = lane >> 1, hf = lane & 1;
+            const int row0 = u < nbox ? pgt[u] * bs + (kt + u * BR) % bs : 0;
+            for (int c = 0; c < C::KS; ++c) {   // the tile's 128-dim chunks
+                const int idx = t * C::KS + c;
+                const int slot = idx % C::NR;
+                if (lane == 0 && !bad) {
                     if (idx >= C::NR)
                         bad = !mbar_wait(bempty + 8 * slot, ((idx / C::NR) - 1) & 1, a.err,
                                          abort_flag);
-                    if (bad) break;
-                    mbar_arrive_expect_tx(bfull + 8 * slot, nbox * BR * 256);
-                    const uint32_t dst = ring0 + slot * C::SLOT;
-                    for (int u = 0; u < nbox; ++u) {
-                        const int row0 = pgt[u] * bs + (kt + u * BR) % bs;
-                        tma_load_3d(dst + u * BR * 128, map, c * 128, cur.h, row0, bfull + 8 * slot,
-                                    pol);
-                        tma_load_3d(dst + C::SUB + u * BR * 128, map, c * 128 + 64, cur.h, row0,
-                                    bfull + 8 * slot, pol);
-                    }
-                    issued = idx + 1;
+                    if (!bad) mbar_arrive_expect_tx(bfull + 8 * slot, nbox * BR * 256);
                 }
+                if (__shfl_sync(0xffffffffu, bad, 0)) break;
+                if (u < nbox)
+                    tma_load_3d(ring0 + slot * C::SLOT + hf * C::SUB + u * BR * 128, map,
+                                c * 128 + hf * 64, cur.h, row0, bfull + 8 * slot, pol);
+                issued = idx + 1;
             }
             if (__shfl_sync(0xffffffffu, bad, 0)) break;
             ++t;

@@ -3,6 +3,7 @@
 // of one attention call.  Everything here is host code except the device
 // error word.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -20,6 +21,10 @@ namespace {
 __device__ int g_error_word;
 
 thread_local char g_last_error[256] = "no error";
+
+// Set by pa_test_expire_next_wait(): the next multi-query launch skips the K
+// loads of each CTA's first tile.
+std::atomic<int> g_expire_next_wait{0};
 
 pa_status cuda_fail(cudaError_t e, const char *where) {
     snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e),
@@ -501,6 +506,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         ta.causal = causal ? 1 : 0;
         ta.box_rows = tc_box;
         ta.err = dev.err;
+        ta.test_skip_first_k = g_expire_next_wait.exchange(0);
         // one CTA per (query block, KV head); virtual block ids: request r owns
         // cu_seqlens_q[r] / bq + r onward
         const int64_t nblk = total_q / bq + num_seqs;
@@ -626,6 +632,8 @@ PA_API pa_status pa_split_kv_reduce(void *out, const float *part_out, const floa
     if (ce != cudaSuccess) return cuda_fail(ce, "split_reduce launch");
     return PA_OK;
 }
+
+PA_API void pa_test_expire_next_wait(void) { g_expire_next_wait.store(1); }
 
 PA_API pa_status pa_device_error(int *code) {
     if (!code) return PA_ERR_INVALID_ARG;

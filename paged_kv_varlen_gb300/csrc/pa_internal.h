@@ -58,6 +58,7 @@ struct TcArgs {
     int causal;
     int box_rows;              // rows per K/V TMA box (divides the tile and the block size)
     int *err;                  // device error word
+    int test_skip_first_k;     // 1: skip the K loads of each CTA's first tile (failure-path test)
 };
 
 // Arguments of the tensor-core kernel for single-query (decode) requests (bf16).

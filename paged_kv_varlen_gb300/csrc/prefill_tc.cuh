@@ -243,18 +243,22 @@ __global__ void __launch_bounds__(352, 1)
             const int kt = tile_of(j) * C::BN;
             const int cnt = min(C::BN, kend - kt);
             const int nsub = (cnt + BR - 1) / BR;
-            if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * st, nsub * C::KCH * BR * 128);
+            // (failure-path test: the K tile 0 is neither armed nor loaded, so the
+            // MMA warp's bounded wait for it runs out)
+            const bool skip = is_k && j == 0 && a.test_skip_first_k;
+            if (lane == 0 && !skip) mbar_arrive_expect_tx(bar_full + 8 * st, nsub * C::KCH * BR * 128);
             __syncwarp();
             const uint32_t dst = stage0 + st * C::KV_TILE;
-            // the tile's boxes are spread over the warp's lanes (lane u issues the
-            // boxes of page run u), so several TMA issues are in flight at once
-            if (lane < nsub) {
-                const int u = lane;
-                const int row0 = pgt[u] * bs + (kt + u * BR) % bs;
-#pragma unroll
-                for (int c = 0; c < C::KCH; ++c)
+            // one box per lane (page run u = lane / KCH, 128-byte chunk lane % KCH):
+            // a box issue holds its warp for ~120 ns, so spreading the tile's
+            // boxes over the lanes keeps many issues in flight
+            {
+                const int u = lane / C::KCH, c = lane % C::KCH;
+                if (u < nsub && !skip) {
+                    const int row0 = pgt[u] * bs + (kt + u * BR) % bs;
                     tma_load_3d(dst + c * C::BN * 128 + u * BR * 128, map, c * 64, h, row0,
                                 bar_full + 8 * st, pol_kv);
+                }
             }
             __syncwarp();
             issued = j + 1;
