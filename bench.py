@@ -54,21 +54,23 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one
-# paged_decode_tc_kernel launch on workload 1, from an ncu capture of the
-# kernel sources whose hash is recorded beside it; reported as null once the
-# sources change, until a new capture is taken.
-NCU_TRAFFIC = {"sources_sha256": "762a3d5dd94725543cbd07b956d98f6bd4e443cec73bf4cf281bb576196db805",
-               "bytes_per_launch": 526379776 + 5281536, "workload": 1,
+# paged_decode_tc_kernel launch on workload 1, from an ncu capture (summary and
+# command in profiles/paged_decode_tc_kernel__gqa_decode_bf16.md) of the
+# kernel sources whose hash is recorded beside it: the files that define that
+# kernel.  Reported as null once they change, until a new capture is taken.
+NCU_TRAFFIC = {"sources_sha256": "d3429d45005de5736aa6f83c597123fbdc0d7f80fa4a1384a92ff3edd2021eeb",
+               "bytes_per_launch": 526309632 + 5093888, "workload": 1,
                "kernel": "paged_decode_tc_kernel"}
+TRAFFIC_SOURCES = ("decode_tc.cuh", "decode_tc_d128.cu", "pa_common.cuh", "tc_common.cuh")
 
 
 def kernel_sources_hash() -> str:
+    """sha256 over the sources of the kernel whose traffic NCU_TRAFFIC holds."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_varlen_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()
 
 

@@ -19,14 +19,17 @@
 //    serves the whole GQA group however small G is; O^T[d x 16] += V^T . P^T
 //    reads the V tile in place as an MN-major A operand.  The CUDA cores only
 //    see G scores per key instead of G * D multiply-adds.
-//  * Warp 4 streams the K tiles (and Q^T once per item), warp 5 the V tiles,
-//    each into its own ring of 32 KB stages (128 keys x 128 dims, the tensor
-//    cores' 128-byte-swizzled layout) by TMA, one box per run of box_rows keys
-//    of a page and 64-dim half.  A 16-token page holds only 2 KB of one head's
-//    K: one thread issuing boxes that small reaches ~26 GB/s per SM, two reach
-//    ~37.  The page ids of each tile reach shared memory by 4-byte cp.async
-//    three tiles ahead and the next request's lengths are loaded a request
-//    ahead, so the producers never wait on a load.
+//  * Warps 4 and 7 stream the K tiles (warp 4 also Q^T once per item), warps
+//    5 and 8 the V tiles, into two rings of 32 KB stages (128 keys x 128
+//    dims, the tensor cores' 128-byte-swizzled layout) by TMA, one box per
+//    run of box_rows keys of a page and 64-dim half; the two warps of a ring
+//    each load half of every stage's page runs, one box per lane.  A 16-token
+//    page holds only 2 KB of one head's K, and issuing a TMA box holds its
+//    warp for ~120 ns: measured on GB300, boxes this small reach ~15 GB/s per
+//    SM from one lane of one warp, ~26 from eight lanes, ~52 from two warps of
+//    eight lanes.  The page ids of each tile reach shared memory by 4-byte
+//    cp.async three tiles ahead and the next request's lengths are loaded a
+//    request ahead, so the producers never wait on a load.
 //  * Warp 6 (MMA) allocates TMEM, issues S^T into one of two TMEM buffers and
 //    O^T into the accumulator of the item's parity; commits release stages.
 //  * Warps 0-3 (one thread per key = TMEM lane): scale S^T into the log2
@@ -72,12 +75,13 @@ struct DtcCfg {
     static constexpr int NBAR = 4 * NR + 7 * 2;
     static constexpr int OFF_RED = OFF_BAR + NBAR * 8;   // float [2][4][8] max, [2][4][8] sum
     static constexpr int PGR = 4;                  // page-id ring of each producer (tiles)
-    static constexpr int OFF_PG = OFF_RED + 2 * 2 * 4 * 8 * 4;   // int [2 producers][PGR][16]
-    static constexpr int OFF_MISC = OFF_PG + 2 * PGR * 16 * 4;
-    static constexpr int THREADS = 224;            // 4 softmax + K + V producer + MMA warps
+    static constexpr int OFF_PG = OFF_RED + 2 * 2 * 4 * 8 * 4;   // int [4 producers][PGR][16]
+    static constexpr int OFF_MISC = OFF_PG + 4 * PGR * 16 * 4;
+    // 4 softmax warps, 2 K and 2 V producer warps, the MMA warp
+    static constexpr int THREADS = 288;
     // batches of at most THREADS requests: their cu_seqlens_q and seq_lens_k,
     // read once by the work-plan scan
-    static constexpr int OFF_LENS = OFF_MISC + 128;   // int [THREADS + 1] cu, int [THREADS] sl
+    static constexpr int OFF_LENS = OFF_MISC + 192;   // int [THREADS + 1] cu, int [THREADS] sl
     static constexpr int SMEM_BYTES = OFF_LENS + (2 * THREADS + 4) * 4 + 1024;   // + alignment slack
     static constexpr int S_COL = 0;                // two S^T buffers of NP columns
     static constexpr int O_COL = 2 * NP;           // two O^T accumulators of KS * NP columns
@@ -268,7 +272,7 @@ __device__ __forceinline__ int64_t dtc_block_scan(int64_t v, long long *scratch,
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(288, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                            const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const DecodeTcArgs a) {
@@ -295,14 +299,14 @@ __global__ void __launch_bounds__(224, 1)
     const uint32_t bar_o_full = bar_o_done + 16;               // [2] item's last PV done
     float *red_max = reinterpret_cast<float *>(smem + C::OFF_RED);   // [2][4 warps][8]
     float *red_sum = red_max + 64;                                   // [2][4 warps][8]
-    int *pgring = reinterpret_cast<int *>(smem + C::OFF_PG);         // [2][PGR][16] page ids
+    int *pgring = reinterpret_cast<int *>(smem + C::OFF_PG);         // [4][PGR][16] page ids
     uint8_t *misc = smem + C::OFF_MISC;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 8);
     int *plan_rk = reinterpret_cast<int *>(misc + 16);               // [4] first item r, k; cut item r, k
-    int *plan_j = reinterpret_cast<int *>(misc + 104);               // [2] j_lo, j_hi
     long long *plan_s = reinterpret_cast<long long *>(misc + 32);    // [2] s_lo, s_hi
-    long long *scratch = reinterpret_cast<long long *>(misc + 48);   // [7]
+    int *plan_j = reinterpret_cast<int *>(misc + 48);                // [2] j_lo, j_hi
+    long long *scratch = reinterpret_cast<long long *>(misc + 64);   // [THREADS / 32]
     int *lens_cu = reinterpret_cast<int *>(smem + C::OFF_LENS);      // [S + 1] when S <= THREADS
     int *lens_sl = lens_cu + C::THREADS + 1;                          // [S]
 
@@ -316,9 +320,9 @@ __global__ void __launch_bounds__(224, 1)
     pdl_trigger();   // the reduce (or the next kernel) may be scheduled meanwhile
     if (tid == 0) {
         for (int s = 0; s < C::NR; ++s) {
-            mbar_init(bar_k_full + 8 * s, 1);   // expect-tx arrival, TMA bytes
+            mbar_init(bar_k_full + 8 * s, 2);   // an expect-tx arrival per producer warp
             mbar_init(bar_k_empty + 8 * s, 1);
-            mbar_init(bar_v_full + 8 * s, 1);
+            mbar_init(bar_v_full + 8 * s, 2);
             mbar_init(bar_v_empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -494,18 +498,21 @@ __global__ void __launch_bounds__(224, 1)
             while (valid(x) && x.ntiles == 0);
         }
     };
-    if (warp == 4 || warp == 5) {
+    if (warp == 4 || warp == 5 || warp == 7 || warp == 8) {
         // ============================================================ producers
-        // Warp 4 streams K (and Q^T once per item), warp 5 streams V, each into
-        // its own ring by TMA: one box per (run of box_rows keys in a page,
-        // 64-dim half).  Lanes fetch the page ids of each tile into a shared
-        // ring by 4-byte cp.async three tiles ahead, so no load is waited on.
-        const bool is_k = warp == 4;
+        // Warps 4 and 7 stream K (warp 4 also Q^T once per item), warps 5 and 8
+        // stream V, into their ring by TMA: one box per (run of box_rows keys in
+        // a page, 64-dim half); warp ph of a ring takes page runs [0, h0) (ph 0)
+        // or [h0, nbox) (ph 1) of every stage.  Lanes fetch the page ids of each
+        // tile into a shared ring by 4-byte cp.async three tiles ahead, so no
+        // load is waited on.
+        const bool is_k = warp == 4 || warp == 7;
+        const int ph = warp >= 7 ? 1 : 0;
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         const uint32_t ring0 = is_k ? kring : vring;
         const uint32_t bfull = is_k ? bar_k_full : bar_v_full;
         const uint32_t bempty = is_k ? bar_k_empty : bar_v_empty;
-        int *pgr = pgring + (is_k ? 0 : C::PGR * 16);
+        int *pgr = pgring + ((is_k ? 0 : 2) + ph) * C::PGR * 16;
         const int bs = a.block_size;
         const int BR = a.box_rows;
         const uint64_t pol = policy_evict_first();   // every K/V byte is read once
@@ -541,7 +548,7 @@ __global__ void __launch_bounds__(224, 1)
             cp_async_wait<C::PGR - 1>();   // tile t's page ids have landed
             __syncwarp();
             int bad = 0;
-            if (lane == 0 && is_k && j == 0) {   // Q^T of the item, rows = its G heads
+            if (lane == 0 && is_k && ph == 0 && j == 0) {   // Q^T of the item: its G heads
                 const int qb = itn & 1;
                 if (itn >= 2)
                     bad = !mbar_wait(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1, a.err,
@@ -559,11 +566,11 @@ __global__ void __launch_bounds__(224, 1)
             const int kt = cur.k0 + j * C::BN;
             const int nbox = (min(C::BN, cur.k1 - kt) + BR - 1) / BR;
             const int *pgt = pgr + (t % C::PGR) * 16;
-            // lane 2u + hf issues the box of page run u, 64-dim half hf: a box
-            // issue holds its warp for ~120 ns, so one box per lane keeps up to
-            // 32 issues in flight (lane 0 alone: ~16 GB/s per warp)
-            const int u = lane >> 1, hf = lane & 1;
-            const int row0 = u < nbox ? pgt[u] * bs + (kt + u * BR) % bs : 0;
+            // lane 2i + hf issues the box of page run u = u0 + i, 64-dim half hf
+            const int h0 = (nbox + 1) >> 1;
+            const int u0 = ph ? h0 : 0, u1 = ph ? nbox : h0;
+            const int u = u0 + (lane >> 1), hf = lane & 1;
+            const int row0 = u < u1 ? pgt[u] * bs + (kt + u * BR) % bs : 0;
             for (int c = 0; c < C::KS; ++c) {   // the tile's 128-dim chunks
                 const int idx = t * C::KS + c;
                 const int slot = idx % C::NR;
@@ -571,10 +578,10 @@ __global__ void __launch_bounds__(224, 1)
                     if (idx >= C::NR)
                         bad = !mbar_wait(bempty + 8 * slot, ((idx / C::NR) - 1) & 1, a.err,
                                          abort_flag);
-                    if (!bad) mbar_arrive_expect_tx(bfull + 8 * slot, nbox * BR * 256);
+                    if (!bad) mbar_arrive_expect_tx(bfull + 8 * slot, (u1 - u0) * BR * 256);
                 }
                 if (__shfl_sync(0xffffffffu, bad, 0)) break;
-                if (u < nbox)
+                if (u < u1)
                     tma_load_3d(ring0 + slot * C::SLOT + hf * C::SUB + u * BR * 128, map,
                                 c * 128 + hf * 64, cur.h, row0, bfull + 8 * slot, pol);
                 issued = idx + 1;

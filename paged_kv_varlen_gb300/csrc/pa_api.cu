@@ -218,10 +218,12 @@ PA_API int pa_choose_partition_size(int num_seqs, int num_kv_heads, int max_seql
 PA_API size_t pa_varlen_attention_workspace_size(int num_seqs, int max_seqlen_k,
                                                  int num_q_heads, int head_dim,
                                                  int partition_size) {
-    if (partition_size < 0 || num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
-    const int P = partition_size > 0 ? partition_size : 256;  // auto picks 0, 256 or 512
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    size_t n = align256(plan_bytes(num_seqs));   // the multi-query kernel's unit plan
+    if (partition_size < 0) return n;
+    const int P = partition_size > 0 ? partition_size : 256;  // auto picks 0, 256, 512 or 1024
     const int max_parts = max_seqlen_k > 0 ? ceil_div(max_seqlen_k, P) : 1;
-    return split_layout(num_seqs, max_parts, num_q_heads, head_dim).total;
+    return n + split_layout(num_seqs, max_parts, num_q_heads, head_dim).total;
 }
 
 PA_API pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t kv_token_stride,
@@ -337,17 +339,26 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
                  "%d split-KV partitions per request, at most %d", max_parts, kMaxReduceParts);
         return PA_ERR_UNSUPPORTED;
     }
-    if (P > 0) {
-        const SplitLayout L = split_layout(num_seqs, max_parts, num_q_heads, head_dim);
-        if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) {
+    // the workspace: the multi-query kernel's unit plan, then the split partials
+    const bool mq_tc = max_seqlen_q > 1 && dtype == PA_BF16;
+    const size_t plan_sz = align256(plan_bytes(num_seqs));
+    int *plan = nullptr;
+    if (mq_tc || P > 0) {
+        const size_t need =
+            plan_sz + (P > 0 ? split_layout(num_seqs, max_parts, num_q_heads, head_dim).total : 0);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) {
             snprintf(g_last_error, sizeof g_last_error,
                      "this call needs %zu bytes of 16-byte aligned workspace (split-KV "
                      "partition %d, %d partitions per request); %zu given%s",
-                     L.total, P, max_parts, workspace ? workspace_bytes : (size_t)0,
+                     need, P, max_parts, workspace ? workspace_bytes : (size_t)0,
                      workspace && !aligned16(workspace) ? " (misaligned)" : "");
             return PA_ERR_WORKSPACE;
         }
-        char *w = static_cast<char *>(workspace);
+        plan = static_cast<int *>(workspace);
+    }
+    if (P > 0) {
+        const SplitLayout L = split_layout(num_seqs, max_parts, num_q_heads, head_dim);
+        char *w = static_cast<char *>(workspace) + plan_sz;
         part_o = reinterpret_cast<float *>(w);
         part_m = reinterpret_cast<float *>(w + L.o_bytes);
         part_l = reinterpret_cast<float *>(w + L.o_bytes + L.ml_bytes);
@@ -478,19 +489,34 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
     }
     // 2) rows of multi-query requests (verify windows, prefill chunks): bf16 on
     //    the tensor cores, float32 on the CUDA-core row kernel
-    if (max_seqlen_q > 1 && dtype == PA_BF16) {
+    if (mq_tc) {
         const int bq = tc_block_rows(group);
-        const int tc_box = gcd_int(tc_tile_keys(head_dim), block_size);
+        // TMA box rows: divide the V sub-tile and the block size, so a box never
+        // crosses a page
+        const int tc_box = gcd_int(tc_vsub_keys(head_dim), block_size);
         CUtensorMap qmap, kmap_tc, vmap_tc;
         st = make_query_map(&qmap, q, head_dim, num_q_heads, total_q, group, bq);
         if (st != PA_OK) return st;
-        // one box per (page, 128-byte chunk)
         st = make_cache_map(&kmap_tc, key_cache, dtype, head_dim, num_kv_heads,
                             num_blocks * block_size, tc_box);
         if (st != PA_OK) return st;
         st = make_cache_map(&vmap_tc, value_cache, dtype, head_dim, num_kv_heads,
                             num_blocks * block_size, tc_box);
         if (st != PA_OK) return st;
+        // 1) the claim order of the work units (one CTA)
+        MqPlanArgs pl;
+        pl.cu_seqlens_q = cu_seqlens_q;
+        pl.seq_lens_k = seq_lens_k;
+        pl.num_seqs = num_seqs;
+        pl.num_kv_heads = num_kv_heads;
+        pl.block_rows = bq;
+        pl.tile_keys = tc_tile_keys(head_dim);
+        pl.max_keys = max_blocks_per_seq * block_size;
+        pl.plan = plan;
+        ce = launch_mq_plan(pl, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "mq_plan launch");
+        // 2) the persistent multi-query kernel: at most one CTA per SM, no more
+        //    than there are units
         TcArgs ta;
         ta.out = out;
         ta.cu_seqlens_q = cu_seqlens_q;
@@ -506,11 +532,10 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         ta.causal = causal ? 1 : 0;
         ta.box_rows = tc_box;
         ta.err = dev.err;
+        ta.plan = plan;
         ta.test_skip_first_k = g_expire_next_wait.exchange(0);
-        // one CTA per (query block, KV head); virtual block ids: request r owns
-        // cu_seqlens_q[r] / bq + r onward
-        const int64_t nblk = total_q / bq + num_seqs;
-        const dim3 grid((unsigned)nblk, num_kv_heads, 1);
+        const int64_t units_max = (total_q / bq + num_seqs) * (int64_t)num_kv_heads;
+        const int grid = (int)std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, units_max);
         switch (head_dim) {
             case 64: ce = launch_prefill_tc_d64(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
             case 128: ce = launch_prefill_tc_d128(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;

@@ -56,10 +56,30 @@ struct TcArgs {
     float qscale;              // scale * log2(e)
     const float *sinks;        // [Hq] or nullptr
     int causal;
-    int box_rows;              // rows per K/V TMA box (divides the tile and the block size)
+    int box_rows;              // rows per K/V TMA box (divides the V sub-tile and the block size)
     int *err;                  // device error word
+    int *plan;                 // claim counter, order and unit prefix (mq_plan_kernel)
     int test_skip_first_k;     // 1: skip the K loads of each CTA's first tile (failure-path test)
 };
+
+// The plan of the multi-query kernel's work units (prefill_plan.cu): in the
+// workspace, [kPlanHeader] header ints (claim counter, requests, units), then
+// order[num_seqs], then P[num_seqs + 1].
+constexpr int kPlanHeader = 4;
+__host__ __device__ constexpr size_t plan_bytes(int num_seqs) {
+    return (size_t)(kPlanHeader + 2 * (size_t)num_seqs + 1) * sizeof(int);
+}
+struct MqPlanArgs {
+    const int32_t *cu_seqlens_q;
+    const int32_t *seq_lens_k;
+    int num_seqs;
+    int num_kv_heads;
+    int block_rows;            // query rows per unit (128 / group)
+    int tile_keys;             // keys per K/V tile
+    int max_keys;              // max_blocks_per_seq * block_size
+    int *plan;
+};
+cudaError_t launch_mq_plan(const MqPlanArgs &a, cudaStream_t stream);
 
 // Arguments of the tensor-core kernel for single-query (decode) requests (bf16).
 struct DecodeTcArgs {
@@ -94,8 +114,10 @@ struct DecodeTcArgs {
     int after_scatter;
 };
 
-// Keys per K/V tile of the tensor-core kernel and query rows per block.
-__host__ __device__ constexpr int tc_tile_keys(int head_dim) { return head_dim >= 256 ? 64 : 128; }
+// Keys per K/V tile of the multi-query kernel, keys of one V sub-tile (the
+// rows a TMA box may span) and query rows per work unit.
+__host__ __device__ constexpr int tc_tile_keys(int head_dim) { return 128; }
+__host__ __device__ constexpr int tc_vsub_keys(int head_dim) { return 8192 / head_dim; }
 __host__ __device__ constexpr int tc_block_rows(int group) { return 128 / group; }
 
 struct ReduceArgs {
@@ -181,12 +203,12 @@ pa_status check_attention_args(const void *out, const void *q, const void *key_c
                                int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                                const float *sinks, int partition_size, pa_dtype dtype);
 
-// Tensor-core kernel for multi-query rows, per head_dim (bf16 only): one CTA
-// per (query block of BQ rows, KV head); grid.x = total_q / BQ + num_seqs
-// virtual blocks, grid.y = num_kv_heads.
+// Tensor-core kernel for multi-query rows, per head_dim (bf16 only):
+// persistent, `grid` CTAs (at most one per SM) claim the work units of the
+// plan written by mq_plan_kernel (launched just before it on the stream).
 #define PA_DECLARE_TC(NAME) \
     cudaError_t NAME(int group, const CUtensorMap &qmap, const CUtensorMap &kmap, \
-                     const CUtensorMap &vmap, const TcArgs &a, dim3 grid, cudaStream_t stream);
+                     const CUtensorMap &vmap, const TcArgs &a, int grid, cudaStream_t stream);
 PA_DECLARE_TC(launch_prefill_tc_d64)
 PA_DECLARE_TC(launch_prefill_tc_d128)
 PA_DECLARE_TC(launch_prefill_tc_d256)

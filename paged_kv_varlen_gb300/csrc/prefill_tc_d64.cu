@@ -5,7 +5,7 @@
 namespace pa {
 
 cudaError_t launch_prefill_tc_d64(int group, const CUtensorMap &qmap, const CUtensorMap &kmap,
-                                  const CUtensorMap &vmap, const TcArgs &a, dim3 grid,
+                                  const CUtensorMap &vmap, const TcArgs &a, int grid,
                                   cudaStream_t stream) {
     return launch_prefill_tc_group<64>(group, qmap, kmap, vmap, a, grid, stream);
 }

@@ -47,15 +47,22 @@ def test_status_strings_and_build_info(lib):
 
 
 def test_workspace_size(lib):
+    # the multi-query kernel's unit plan comes first: 4 header ints, then
+    # order[S] and P[S + 1] (ints), rounded up to 256 bytes
+    plan = (4 + 2 * 4 + 1) * 4
+    plan = (plan + 255) // 256 * 256
     # forced P = 512: 4 seqs x ceil(8192/512)=16 parts x 32 heads x (128 + 2) floats
     # plus one extra partial slot (8 heads x (128 + 2) floats) per decode CTA
     # (256 at most) for items cut between CTAs, and their 16-byte table entries
     n = lib.pa_varlen_attention_workspace_size(4, 8192, 32, 128, 512)
     units = 4 * 16 * 32
     extra = 256 * 8 * (128 + 2) * 4 + 256 * 16
-    assert n >= units * (128 + 2) * 4 + extra
-    assert n < units * (128 + 2) * 4 + extra + 6 * 256
-    assert lib.pa_varlen_attention_workspace_size(4, 8192, 32, 128, -1) == 0
+    assert n >= plan + units * (128 + 2) * 4 + extra
+    assert n < plan + units * (128 + 2) * 4 + extra + 6 * 256
+    # no split: the plan alone
+    assert lib.pa_varlen_attention_workspace_size(4, 8192, 32, 128, -1) == plan
+    big = lib.pa_varlen_attention_workspace_size(65535, 0, 32, 128, -1)
+    assert big == ((4 + 2 * 65535 + 1) * 4 + 255) // 256 * 256
     # auto is bounded by the smallest partition it may choose (256)
     assert (lib.pa_varlen_attention_workspace_size(4, 8192, 32, 128, 0)
             >= lib.pa_varlen_attention_workspace_size(4, 8192, 32, 128, 256))
