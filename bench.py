@@ -465,6 +465,7 @@ def measure(args, widx, rank, world, local, with_cpu_baseline):
     e1.record(stream)
     e1.synchronize()
     barrier()
+    assert pa.pa_device_error() == 0, "device error word set during the end-to-end steps"
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device) / steps
     e2e_value, _ = metric_value(kind, work, e2e_s, world)
 

@@ -253,9 +253,11 @@ pa_status pa_varlen_attention_static_scratch(
 
 /*
  * Reads and clears the library's device-side error word for the current
- * device (synchronises the device).  Nonzero means a kernel gave up on a
- * bounded wait (a pipeline barrier that never completed); its output is then
- * unreliable.  Returns PA_OK, or PA_ERR_CUDA if the read failed.
+ * device (synchronises the device).  Nonzero means a kernel gave up: 1 = a
+ * bounded wait ran out (a pipeline barrier that never completed), 3 = the
+ * multi-query kernel met a work unit outside the batch (an inconsistent plan)
+ * and skipped it; the output is then unreliable.  Returns PA_OK, or
+ * PA_ERR_CUDA if the read failed.
  */
 pa_status pa_device_error(int *code);
 

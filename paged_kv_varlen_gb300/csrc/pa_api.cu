@@ -534,6 +534,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         ta.err = dev.err;
         ta.plan = plan;
         ta.test_skip_first_k = g_expire_next_wait.exchange(0);
+        ta.total_q = total_q;
         const int64_t units_max = (total_q / bq + num_seqs) * (int64_t)num_kv_heads;
         const int grid = (int)std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, units_max);
         switch (head_dim) {

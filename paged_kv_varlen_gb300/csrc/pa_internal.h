@@ -60,6 +60,7 @@ struct TcArgs {
     int *err;                  // device error word
     int *plan;                 // claim counter, order and unit prefix (mq_plan_kernel)
     int test_skip_first_k;     // 1: skip the K loads of each CTA's first tile (failure-path test)
+    int64_t total_q;           // packed query rows (bounds of the output writes)
 };
 
 // The plan of the multi-query kernel's work units (prefill_plan.cu): in the

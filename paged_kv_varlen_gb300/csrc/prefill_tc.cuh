@@ -81,6 +81,10 @@ struct MqCfg {
     static constexpr int Q_BYTES = KCH * 128 * 128;     // [KCH][128 rows][128 B]
     static constexpr int NSLOT = D >= 128 ? 10 : 12;
     static constexpr int NU = 8;                        // unit ring entries
+    // With one Q buffer the next unit's Q lands only after the previous
+    // unit's last S, so at a unit boundary the MMAs take the previous unit's
+    // last PV first (ring order "V before K" there, see mq_pos_k).
+    static constexpr bool PV_FIRST = NQB == 1;
     static constexpr int OFF_SLOT = NQB * Q_BYTES;
     static constexpr int OFF_BAR = OFF_SLOT + NSLOT * SLOT;
     static constexpr int NBAR = 2 * NQB + 2 * NSLOT + 6 + NOB + 2 * NU;
@@ -88,7 +92,11 @@ struct MqCfg {
     static constexpr int OFF_UNIT = OFF_RED + 2 * 128 * 4;              // MqUnit [NU]
     static constexpr int OFF_MISC = OFF_UNIT + NU * (int)sizeof(MqUnit);   // TMEM base, abort
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;             // + alignment slack
-    static constexpr int THREADS = 448;
+    static constexpr int NPROD = 6;                     // producer warps
+    static constexpr int W_MMA = 8 + NPROD;             // MMA-issuing warp
+    static constexpr int W_SCHED = 9 + NPROD;           // scheduler warp
+    static constexpr int THREADS = 32 * (10 + NPROD);
+    static_assert(THREADS == 512, "launch bounds below");
     static constexpr int TMEM_COLS = 512;
     static constexpr int O_COL = 2 * BN;                // after the two S buffers
     static_assert(VKEYS * 128 * KCH == SLOT, "a V sub-tile fills a slot");
@@ -97,11 +105,22 @@ struct MqCfg {
     static_assert(Q_BYTES % 1024 == 0 && SLOT % 1024 == 0, "swizzle atoms");
 };
 
-// Ring positions (in sub-tiles) of the CTA's tile t: K(t) first, V(t) after
-// K(t + 1); after the last tile the producers add an empty K so that this
-// holds for every tile.
-__device__ __forceinline__ int mq_pos_k(int t, int sub) { return t == 0 ? 0 : (2 * t - 1) * sub; }
-__device__ __forceinline__ int mq_pos_v(int t, int sub) { return (2 * t + 2) * sub; }
+// Ring positions (in sub-tiles) of the CTA's tile t.  The producers fill the
+// ring, and the MMAs free it, in one and the same order: the parity waits on
+// a slot's barriers assume that position p is freed before p + 1 (a slot is
+// re-armed only after the position NSLOT before it is freed, and the wait
+// cannot tell that phase from the one NSLOT earlier).  Tile t >= 1 owns the
+// group of 2 SUB positions starting at (2t - 1) SUB: K(t) then V(t - 1)
+// inside a unit, V(t - 1) then K(t) at a unit's first tile when pv_first (the
+// MMAs take the previous unit's last PV before the new unit's first S).
+// After the last tile: V(last) -- preceded by an empty K when !pv_first, so
+// that V(t) always sits at (2t + 2) SUB.
+__device__ __forceinline__ int mq_pos_k(int t, int sub, bool pv_first, bool unit_first) {
+    return t == 0 ? 0 : (2 * t - 1) * sub + (pv_first && unit_first ? sub : 0);
+}
+__device__ __forceinline__ int mq_pos_v(int t, int sub, bool pv_first, bool unit_last) {
+    return pv_first ? (2 * t + 1) * sub + (unit_last ? 0 : sub) : (2 * t + 2) * sub;
+}
 
 // Or over `nthreads` threads of named barrier `id` (all of them get the result).
 __device__ __forceinline__ bool barrier_or(int id, int nthreads, bool v) {
@@ -118,7 +137,7 @@ __device__ __forceinline__ bool barrier_or(int id, int nthreads, bool v) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(512, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                             const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const TcArgs a) {
@@ -168,12 +187,12 @@ __global__ void __launch_bounds__(448, 1)
         for (int b = 0; b < C::NOB; ++b) mbar_init(bar_o_free + 8 * b, 8);
         for (int u = 0; u < C::NU; ++u) {
             mbar_init(bar_u_full + 8 * u, 1);
-            mbar_init(bar_u_empty + 8 * u, 13);
+            mbar_init(bar_u_empty + 8 * u, 9 + C::NPROD);   // every role but the scheduler
         }
         fence_barrier_init();
         *abort_flag = 0;
     }
-    if (warp == 12) {
+    if (warp == C::W_MMA) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -202,7 +221,7 @@ __global__ void __launch_bounds__(448, 1)
     };
     auto tile_of = [](const MqUnit &, int j) { return j; };
 
-    if (warp == 13) {
+    if (warp == C::W_SCHED) {
         // ============================================================ scheduler
         if (lane == 0) {
             prefetch_tensormap(&qmap);
@@ -247,6 +266,13 @@ __global__ void __launch_bounds__(448, 1)
                     u.kend = max(0, a.causal ? min(u.N, u.N - n + u.i0 + u.rows) : u.N);
                     u.ntiles = (u.kend + C::BN - 1) / C::BN;
                     u.reuse = nblk > 1;
+                    // a unit outside the batch (an inconsistent plan) is never
+                    // published: report it and stop claiming
+                    if (r < 0 || r >= a.num_seqs || c0 < 0 || n < 2 || c0 + n > a.total_q ||
+                        u.i0 < 0 || u.rows < 1) {
+                        report_error(a.err, 3);
+                        u.r = -1;
+                    }
                 }
                 units[us] = u;
                 mbar_arrive(bar_u_full + 8 * us);   // (release: the unit is visible)
@@ -271,7 +297,7 @@ __global__ void __launch_bounds__(448, 1)
                 if (q_last[b] >= 0)
                     mbar_drain(bar_q_full + 8 * b, (q_last[b] / C::NQB) & 1, kWaitLimitCycles / 8);
         }
-    } else if (warp >= 8 && warp < 12) {
+    } else if (warp >= 8 && warp < 8 + C::NPROD) {
         // ============================================================ producers
         // Sub-tile at ring position seq belongs to warp seq % 4: that warp alone
         // waits for its slot, arms it with the sub-tile's bytes and issues its
@@ -307,7 +333,7 @@ __global__ void __launch_bounds__(448, 1)
         // keys, KV head h: one box per page run, lane u loads run u; pg: this
         // lane's page id of page run `lane`
         auto issue_k = [&](int s, int h, int kt, int cnt, int pg, bool skip) {
-            if ((seq & 3) == pw) {
+            if (seq % C::NPROD == pw) {
                 const int nbox = (cnt + BR - 1) / BR;   // <= 16
                 const uint32_t slot = acquire(nbox * BR * 128, !skip);
                 if (!bad && !skip && lane < nbox)
@@ -327,7 +353,7 @@ __global__ void __launch_bounds__(448, 1)
             const int ul = lane / C::KCH, ch = lane % C::KCH;
             const int u = u_lo + ul;
             const int pgu = __shfl_sync(0xffffffffu, pg, u & 31);
-            if ((seq & 3) == pw) {
+            if (seq % C::NPROD == pw) {
                 const uint32_t slot = acquire(nbox * BR * 128, true);
                 if (!bad && lane < nbox)
                     tma_load_3d(slot0 + slot * C::SLOT + ch * (C::VKEYS * 128) + ul * BR * 128,
@@ -362,10 +388,18 @@ __global__ void __launch_bounds__(448, 1)
                 // (failure-path test: the CTA's first K tile is neither armed
                 // nor loaded, so the MMA warp's bounded wait for it runs out)
                 const bool skip = t == 0 && a.test_skip_first_k;
-                for (int s = 0; s < C::SUB && !bad; ++s) issue_k(s, u.h, kt, cnt, pg_cur, skip);
-                if (prev)
+                if (C::PV_FIRST && j == 0 && prev) {   // unit boundary: V(t - 1), then K(t)
                     for (int s = 0; s < C::SUB && !bad; ++s)
                         issue_v(s, prev_h, prev_kt, prev_cnt, prev_pg);
+                    for (int s = 0; s < C::SUB && !bad; ++s)
+                        issue_k(s, u.h, kt, cnt, pg_cur, skip);
+                } else {
+                    for (int s = 0; s < C::SUB && !bad; ++s)
+                        issue_k(s, u.h, kt, cnt, pg_cur, skip);
+                    if (prev)
+                        for (int s = 0; s < C::SUB && !bad; ++s)
+                            issue_v(s, prev_h, prev_kt, prev_cnt, prev_pg);
+                }
                 prev = 1;
                 prev_h = u.h;
                 prev_kt = kt;
@@ -376,17 +410,18 @@ __global__ void __launch_bounds__(448, 1)
                 ++t;
             }
         }
-        // an empty K after the last tile (no boxes: the slot completes on its
-        // owner's arrival alone), then its V
+        // after the last tile its V, preceded when !PV_FIRST by an empty K (no
+        // boxes: the slot completes on its owner's arrival alone)
         if (prev && !bad) {
-            for (int s = 0; s < C::SUB && !bad; ++s) issue_k(s, 0, 0, 0, 0, false);
+            if (!C::PV_FIRST)
+                for (int s = 0; s < C::SUB && !bad; ++s) issue_k(s, 0, 0, 0, 0, false);
             for (int s = 0; s < C::SUB && !bad; ++s) issue_v(s, prev_h, prev_kt, prev_cnt, prev_pg);
         }
         // copies in flight land before the CTA can exit (bounded)
         if (lane == 0)
             for (int i = max(0, seq - C::NSLOT); i < seq; ++i)
                 mbar_drain(bar_full + 8 * (i % C::NSLOT), (i / C::NSLOT) & 1, kWaitLimitCycles / 8);
-    } else if (warp == 12) {
+    } else if (warp == C::W_MMA) {
         // ============================================================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, C::BN, 0, 0);
@@ -394,13 +429,13 @@ __global__ void __launch_bounds__(448, 1)
             int t = 0, itn = 0;
             uint32_t last_commit = 0, last_parity = 0;   // drained before TMEM is freed
             bool any = false;
-            // the PV of tile tp (cnt keys) into accumulator ob; first: the unit's
-            // first tile (overwrite O); itn_p: the unit's number
-            auto issue_pv = [&](int tp, int cnt, int ob, bool first, int itn_p) {
+            // the PV of tile tp (cnt keys) into accumulator ob; first / last: the
+            // unit's first (overwrite O) / last tile; itn_p: the unit's number
+            auto issue_pv = [&](int tp, int cnt, int ob, bool first, bool last, int itn_p) {
                 if (first && itn_p >= C::NOB)   // the unit NOB back has read its O out
                     mbar_wait(bar_o_free + 8 * ob, ((itn_p / C::NOB) - 1) & 1, a.err, abort_flag);
                 mbar_wait(bar_p_full + 8 * (tp & 1), (tp >> 1) & 1, a.err, abort_flag);
-                const int p0 = mq_pos_v(tp, C::SUB);
+                const int p0 = mq_pos_v(tp, C::SUB, C::PV_FIRST, last);
                 const int nk = (cnt + 15) / 16;   // 16-key steps holding keys
                 const uint32_t pt = tmem + (tp & 1) * C::BN;
                 constexpr int KPS = C::VKEYS / 16;   // steps per V sub-tile
@@ -430,7 +465,7 @@ __global__ void __launch_bounds__(448, 1)
                 last_parity = (tp >> 1) & 1;
                 any = true;
             };
-            bool pv_pending = false, pv_first = false;
+            bool pv_pending = false, pv_first = false, pv_last = false;
             int pv_t = 0, pv_cnt = 0, pv_ob = 0, pv_itn = 0;
             for (int k = 0;; ++k) {
                 MqUnit u;
@@ -440,10 +475,11 @@ __global__ void __launch_bounds__(448, 1)
                 if (u.ntiles == 0) continue;
                 const int qb = itn % C::NQB;
                 const int ob = itn % C::NOB;
-                // the previous unit's last PV goes first when this unit's Q has
-                // not landed yet (its epilogue need not wait for the Q load)
-                if (pv_pending && !mbar_try_wait(bar_q_full + 8 * qb, (itn / C::NQB) & 1)) {
-                    issue_pv(pv_t, pv_cnt, pv_ob, pv_first, pv_itn);
+                // one Q buffer: the previous unit's last PV goes first (its
+                // epilogue need not wait for this unit's Q load); the order is
+                // fixed, as the ring's (mq_pos_k)
+                if (C::PV_FIRST && pv_pending) {
+                    issue_pv(pv_t, pv_cnt, pv_ob, pv_first, pv_last, pv_itn);
                     pv_pending = false;
                 }
                 mbar_wait(bar_q_full + 8 * qb, (itn / C::NQB) & 1, a.err, abort_flag);
@@ -452,7 +488,7 @@ __global__ void __launch_bounds__(448, 1)
                     const int sb = t & 1;
                     // S(t) = Q K(t)^T into buffer sb (its last reader, PV(t - 2),
                     // was issued before by this thread)
-                    const int p0 = mq_pos_k(t, C::SUB);
+                    const int p0 = mq_pos_k(t, C::SUB, C::PV_FIRST, j == 0);
 #pragma unroll
                     for (int s = 0; s < C::SUB; ++s) {   // 64-dim chunk s of K and Q
                         const int slot = (p0 + s) % C::NSLOT;
@@ -473,27 +509,30 @@ __global__ void __launch_bounds__(448, 1)
                     }
                     tc_commit(bar_s_full + 8 * sb);
                     if (j == u.ntiles - 1) tc_commit(bar_q_empty + 8 * qb);
-                    if (pv_pending) issue_pv(pv_t, pv_cnt, pv_ob, pv_first, pv_itn);
+                    if (pv_pending) issue_pv(pv_t, pv_cnt, pv_ob, pv_first, pv_last, pv_itn);
                     pv_pending = true;
                     pv_t = t;
                     pv_cnt = min(C::BN, u.kend - tile_of(u, j) * C::BN);
                     pv_ob = ob;
                     pv_first = j == 0;
+                    pv_last = j == u.ntiles - 1;
                     pv_itn = itn;
                     ++t;
                 }
                 ++itn;
             }
             if (pv_pending) {
-                // the producers' empty K after the last tile: release its slots
-                const int p0 = mq_pos_k(t, C::SUB);
+                if (!C::PV_FIRST) {
+                    // the producers' empty K after the last tile: release its slots
+                    const int p0 = mq_pos_k(t, C::SUB, false, false);
 #pragma unroll
-                for (int s = 0; s < C::SUB; ++s) {
-                    mbar_wait(bar_full + 8 * ((p0 + s) % C::NSLOT), ((p0 + s) / C::NSLOT) & 1,
-                              a.err, abort_flag);
-                    mbar_arrive(bar_empty + 8 * ((p0 + s) % C::NSLOT));
+                    for (int s = 0; s < C::SUB; ++s) {
+                        mbar_wait(bar_full + 8 * ((p0 + s) % C::NSLOT),
+                                  ((p0 + s) / C::NSLOT) & 1, a.err, abort_flag);
+                        mbar_arrive(bar_empty + 8 * ((p0 + s) % C::NSLOT));
+                    }
                 }
-                issue_pv(pv_t, pv_cnt, pv_ob, pv_first, pv_itn);
+                issue_pv(pv_t, pv_cnt, pv_ob, pv_first, pv_last, pv_itn);
             }
             // every MMA is finished before TMEM is freed (bounded, also when
             // the pipeline was aborted)
@@ -527,7 +566,7 @@ __global__ void __launch_bounds__(448, 1)
             if (lane == 0) mbar_arrive(bar_u_empty + 8 * (k % C::NU));
             // one decision for all 256 threads: the named barriers below stay matched
             if (barrier_or(2, 256, !ok || u.r < 0)) break;
-            const bool row_ok = (m < C::M_USED) && (i < u.rows);
+            const bool row_ok = (m < C::M_USED) && (i < u.rows) && u.c0 + u.i0 + i < a.total_q;
             const int qi = u.i0 + i;
             const int N = u.N, n = u.n;
             const int lim = min(N - 1, a.causal ? N - n + qi : N - 1);   // last visible key
@@ -580,13 +619,15 @@ __global__ void __launch_bounds__(448, 1)
                 const int cnt = min(C::BN, u.kend - kt0);
                 if (cnt & 15) {
                     const int s_v = cnt / C::VKEYS;                  // V sub-tile holding them
-                    const int pos = mq_pos_v(t, C::SUB) + s_v;
+                    const int pos = mq_pos_v(t, C::SUB, C::PV_FIRST, j == u.ntiles - 1) + s_v;
                     // A parity wait is only meaningful while the barrier is at most
                     // one phase away.  Once S(t) is done every MMA before it is done
                     // too, so the slot's previous use is complete -- unless it is
-                    // the V of tile t - 1 (D = 256, V sub-tiles 2 and 3), whose PV
-                    // may still run: wait for that PV first.
-                    if (t >= 1 && pos - C::NSLOT >= mq_pos_v(t - 1, C::SUB))
+                    // the V of tile t - 1, whose PV may still run: wait for that PV
+                    // first.  (With the ring sizes used, the previous use is never
+                    // that V; the wait keeps the rule true for any size.)
+                    const int pv1 = t >= 1 ? mq_pos_v(t - 1, C::SUB, C::PV_FIRST, j == 0) : 0;
+                    if (t >= 1 && pos - C::NSLOT >= pv1 && pos - C::NSLOT < pv1 + C::SUB)
                         mbar_wait(bar_o_done + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, a.err,
                                   abort_flag);
                     mbar_wait(bar_full + 8 * (pos % C::NSLOT), (pos / C::NSLOT) & 1, a.err,
@@ -710,7 +751,7 @@ __global__ void __launch_bounds__(448, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 12) {
+    if (warp == C::W_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }

@@ -31,7 +31,10 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const Redu
     const int Hq = a.num_q_heads;
     if (!a.meta_before_wait) pdl_wait();   // (launched early: see launch_reduce_t)
     const int c0 = a.cu_seqlens_q[r];
-    if (a.cu_seqlens_q[r + 1] - c0 != 1) return;
+    if (a.cu_seqlens_q[r + 1] - c0 != 1) {
+        if (a.meta_before_wait) pdl_wait();   // complete only after the kernel before it
+        return;
+    }
     const int N = max(0, a.seq_lens_k[r]);
     const int nparts = min((N + a.partition_size - 1) / a.partition_size, a.max_parts);
     const int tid = threadIdx.x;
