@@ -7,7 +7,7 @@
 // keys, causal rows bottom-right aligned (row i sees keys j <= N - n + i),
 // with the sink logit of each head counted once in the denominator.
 //
-// GB300 design (one CTA per SM, 448 threads, 14 warps):
+// GB300 design (one CTA per SM, 480 threads, 15 warps):
 //  * A work unit is (request, KV head, query block of BQ = 128 / G rows): its
 //    MMA rows are the (query row, head) pairs of the G heads that share the
 //    KV head, so every K/V page read serves the whole GQA group.  CTAs claim
@@ -15,31 +15,28 @@
 //    mq_plan_kernel), so no SM idles while heavy units wait.
 //  * The CTA's units form one stream of 128-key tiles t = 0, 1, ...: the
 //    tensor cores compute S(t) = Q K(t)^T into one of two TMEM buffers while
-//    the softmax of tile t - 1 runs, then O += P(t-1) V(t-1); loads, MMAs and
+//    the softmax of tile t - 1 runs, and O += P(t-1) V(t-1); loads, MMAs and
 //    the softmax run across unit boundaries without draining.
-//  * Warp 13 (scheduler) claims units, publishes them in a ring of NU
+//  * Warp 14 (scheduler) claims units, publishes them in a ring of NU
 //    entries, and loads each unit's Q (TMA, 3-D box over [total_q, H_q, D])
 //    into one of NQB buffers.
-//  * Warps 8-11 (producers) stream K and V through one ring of NSLOT 16 KB
-//    sub-tiles, in the order the MMAs read them: K(t), then V(t-1).  A K
-//    sub-tile is one 64-dim chunk of the tile's 128 keys, a V sub-tile
-//    128 / (D / 64) keys of every dimension; each MMA group waits for its own
-//    sub-tile and frees it as soon as it is done, so loads overlap the MMAs
-//    at a fine grain.  A sub-tile's TMA boxes (a page run of box_rows keys x
-//    64 dims, 128-byte swizzled) are issued by one of the four warps (round
-//    robin), one box per lane: issuing a box holds its warp for ~80-120 ns,
-//    so the four warps load four sub-tiles at once (~100 GB/s per SM from
-//    L2 with 2 KB boxes).  K/V of a
-//    request whose rows fit one unit is read once per head and marked
-//    evict-first; longer requests' K/V is re-read by their other units and
-//    kept (evict-last); the units of one request and head walk the tiles in
-//    the same order, so they read each tile at about the same time.
-//  * Warp 12 (MMA) allocates the 512 TMEM columns -- S buffers [0, 256), O
-//    accumulators from 256 -- issues the MMAs from one thread and commits
-//    them to mbarriers.  P is written by the softmax over its own S columns
-//    (bf16, two per column) and read by the PV MMA as its A operand from
-//    TMEM; S(t + 2) reuses the buffer only after PV(t) (same issuing thread,
-//    in order).
+//  * Warps 8-9 fill a ring of NKS 16 KB K sub-tiles (one 64-dim chunk of a
+//    tile's 128 keys), warps 10-11 a ring of NVS V sub-tiles (128 / (D / 64)
+//    keys of every dimension).  A sub-tile's TMA boxes (a page run of box_rows
+//    keys x 64 dims, 128-byte swizzled) are issued by one warp of its ring
+//    (round robin), one box per lane.  K/V of a request whose rows fit one
+//    unit is read once per head and marked evict-first; longer requests' K/V
+//    is re-read by their other units and kept (evict-last).
+//  * The tensor cores are fed by two issuing threads: tcgen05.mma issue
+//    blocks while the MMA queue is full, so a thread waiting on a barrier
+//    leaves the tensor pipe idle.  Warp 12 issues S(t) once K(t) has landed
+//    and PV(t - NSB) has read P(t - NSB) out of its TMEM buffer; warp 13 issues
+//    PV(t) once the softmax has written P(t) and V(t) has landed.  Each ring
+//    is freed by its own issuer in the order it is filled, which is what the
+//    parity waits on its barriers rely on.  Warp 12 owns the 512 TMEM columns
+//    -- S buffers [0, 256), O accumulators from 256.  P is written by the
+//    softmax over its own S columns (bf16, two per column) and read by the PV
+//    MMA as its A operand from TMEM.
 //  * Warps 0-7 (two softmax warpgroups, one thread per TMEM lane = MMA row;
 //    warpgroup w takes keys [64 w, 64 w + 64) of every tile): mask, scale into
 //    the log2 domain, exchange row maxima through shared memory, rescale O
@@ -77,50 +74,33 @@ struct MqCfg {
     static constexpr int SLOT = BN * 128;               // bytes of a ring slot (16 KB)
     static constexpr int VKEYS = BN / SUB;              // keys of a V sub-tile
     static constexpr int NQB = D >= 256 ? 1 : 2;        // Q buffers
-    static constexpr int NOB = D >= 256 ? 1 : 2;        // O accumulators
+    static constexpr int NSB = D >= 256 ? 2 : 3;        // S/P buffers in TMEM
+    static constexpr int NOB = D <= 64 ? 2 : 1;         // O accumulators
     static constexpr int Q_BYTES = KCH * 128 * 128;     // [KCH][128 rows][128 B]
-    static constexpr int NSLOT = D >= 128 ? 10 : 12;
+    static constexpr int NKS = D >= 128 ? 5 : 6;         // K ring slots
+    static constexpr int NVS = NKS;                      // V ring slots
     static constexpr int NU = 8;                        // unit ring entries
-    // With one Q buffer the next unit's Q lands only after the previous
-    // unit's last S, so at a unit boundary the MMAs take the previous unit's
-    // last PV first (ring order "V before K" there, see mq_pos_k).
-    static constexpr bool PV_FIRST = NQB == 1;
     static constexpr int OFF_SLOT = NQB * Q_BYTES;
-    static constexpr int OFF_BAR = OFF_SLOT + NSLOT * SLOT;
-    static constexpr int NBAR = 2 * NQB + 2 * NSLOT + 6 + NOB + 2 * NU;
+    static constexpr int OFF_VSLOT = OFF_SLOT + NKS * SLOT;
+    static constexpr int OFF_BAR = OFF_VSLOT + NVS * SLOT;
+    static constexpr int NBAR = 2 * NQB + 2 * NKS + 2 * NVS + 3 * NSB + NOB + 2 * NU;
     static constexpr int OFF_RED = OFF_BAR + ((NBAR * 8 + 15) & ~15);   // float [2][128]
     static constexpr int OFF_UNIT = OFF_RED + 2 * 128 * 4;              // MqUnit [NU]
     static constexpr int OFF_MISC = OFF_UNIT + NU * (int)sizeof(MqUnit);   // TMEM base, abort
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;             // + alignment slack
-    static constexpr int NPROD = 6;                     // producer warps
-    static constexpr int W_MMA = 8 + NPROD;             // MMA-issuing warp
-    static constexpr int W_SCHED = 9 + NPROD;           // scheduler warp
-    static constexpr int THREADS = 32 * (10 + NPROD);
-    static_assert(THREADS == 512, "launch bounds below");
+    static constexpr int NPK = 2, NPV = 2;               // K and V producer warps
+    static constexpr int W_MMA_S = 8 + NPK + NPV;       // S-issuing warp (TMEM owner)
+    static constexpr int W_MMA_PV = W_MMA_S + 1;        // PV-issuing warp
+    static constexpr int W_SCHED = W_MMA_S + 2;         // scheduler warp
+    static constexpr int THREADS = 32 * (W_SCHED + 1);
+    static_assert(THREADS == 480, "launch bounds below");
     static constexpr int TMEM_COLS = 512;
-    static constexpr int O_COL = 2 * BN;                // after the two S buffers
+    static constexpr int O_COL = NSB * BN;              // after the S buffers
     static_assert(VKEYS * 128 * KCH == SLOT, "a V sub-tile fills a slot");
     static_assert(O_COL + NOB * D <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(Q_BYTES % 1024 == 0 && SLOT % 1024 == 0, "swizzle atoms");
 };
-
-// Ring positions (in sub-tiles) of the CTA's tile t.  The producers fill the
-// ring, and the MMAs free it, in one and the same order: the parity waits on
-// a slot's barriers assume that position p is freed before p + 1 (a slot is
-// re-armed only after the position NSLOT before it is freed, and the wait
-// cannot tell that phase from the one NSLOT earlier).  Tile t >= 1 owns the
-// group of 2 SUB positions starting at (2t - 1) SUB: K(t) then V(t - 1)
-// inside a unit, V(t - 1) then K(t) at a unit's first tile when pv_first (the
-// MMAs take the previous unit's last PV before the new unit's first S).
-// After the last tile: V(last) -- preceded by an empty K when !pv_first, so
-// that V(t) always sits at (2t + 2) SUB.
-__device__ __forceinline__ int mq_pos_k(int t, int sub, bool pv_first, bool unit_first) {
-    return t == 0 ? 0 : (2 * t - 1) * sub + (pv_first && unit_first ? sub : 0);
-}
-__device__ __forceinline__ int mq_pos_v(int t, int sub, bool pv_first, bool unit_last) {
-    return pv_first ? (2 * t + 1) * sub + (unit_last ? 0 : sub) : (2 * t + 2) * sub;
-}
 
 // Or over `nthreads` threads of named barrier `id` (all of them get the result).
 __device__ __forceinline__ bool barrier_or(int id, int nthreads, bool v) {
@@ -137,7 +117,7 @@ __device__ __forceinline__ bool barrier_or(int id, int nthreads, bool v) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(480, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                             const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const TcArgs a) {
@@ -147,16 +127,19 @@ __global__ void __launch_bounds__(512, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t q_smem = sbase;
-    const uint32_t slot0 = sbase + C::OFF_SLOT;
+    const uint32_t kring0 = sbase + C::OFF_SLOT;                      // K ring [NKS][16 KB]
+    const uint32_t vring0 = sbase + C::OFF_VSLOT;                     // V ring [NVS][16 KB]
     // barriers (each waited by its parties in order, never two phases behind)
     const uint32_t bar_q_full = sbase + C::OFF_BAR;                   // [NQB]
     const uint32_t bar_q_empty = bar_q_full + 8 * C::NQB;             // [NQB] last S of the unit done
-    const uint32_t bar_full = bar_q_empty + 8 * C::NQB;               // [NSLOT] owner's arrival + bytes
-    const uint32_t bar_empty = bar_full + 8 * C::NSLOT;               // [NSLOT] its MMAs done
-    const uint32_t bar_s_full = bar_empty + 8 * C::NSLOT;             // [2] S(t) in TMEM
-    const uint32_t bar_p_full = bar_s_full + 16;                      // [2] P(t) in TMEM (8 warps)
-    const uint32_t bar_o_done = bar_p_full + 16;                      // [2] PV(t) done
-    const uint32_t bar_o_free = bar_o_done + 16;                      // [NOB] O read out (8 warps)
+    const uint32_t bar_kfull = bar_q_empty + 8 * C::NQB;              // [NKS] owner's arrival + bytes
+    const uint32_t bar_kempty = bar_kfull + 8 * C::NKS;               // [NKS] its S MMAs done
+    const uint32_t bar_vfull = bar_kempty + 8 * C::NKS;               // [NVS] owner's arrival + bytes
+    const uint32_t bar_vempty = bar_vfull + 8 * C::NVS;               // [NVS] its PV MMAs done
+    const uint32_t bar_s_full = bar_vempty + 8 * C::NVS;              // [NSB] S(t) in TMEM
+    const uint32_t bar_p_full = bar_s_full + 8 * C::NSB;              // [NSB] P(t) in TMEM (8 warps)
+    const uint32_t bar_o_done = bar_p_full + 8 * C::NSB;              // [NSB] PV(t) done
+    const uint32_t bar_o_free = bar_o_done + 8 * C::NSB;              // [NOB] O read out (8 warps)
     const uint32_t bar_u_full = bar_o_free + 8 * C::NOB;              // [NU] unit published
     const uint32_t bar_u_empty = bar_u_full + 8 * C::NU;              // [NU] unit read (13 warps)
     float *xr = reinterpret_cast<float *>(smem + C::OFF_RED);         // [2][128]
@@ -175,11 +158,15 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(bar_q_full + 8 * b, 1);
             mbar_init(bar_q_empty + 8 * b, 1);
         }
-        for (int s = 0; s < C::NSLOT; ++s) {
-            mbar_init(bar_full + 8 * s, 1);   // the owning producer warp's arrival
-            mbar_init(bar_empty + 8 * s, 1);
+        for (int s = 0; s < C::NKS; ++s) {
+            mbar_init(bar_kfull + 8 * s, 1);   // the owning producer warp's arrival
+            mbar_init(bar_kempty + 8 * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int s = 0; s < C::NVS; ++s) {
+            mbar_init(bar_vfull + 8 * s, 1);
+            mbar_init(bar_vempty + 8 * s, 1);
+        }
+        for (int b = 0; b < C::NSB; ++b) {
             mbar_init(bar_s_full + 8 * b, 1);
             mbar_init(bar_p_full + 8 * b, 8);
             mbar_init(bar_o_done + 8 * b, 1);
@@ -187,12 +174,12 @@ __global__ void __launch_bounds__(512, 1)
         for (int b = 0; b < C::NOB; ++b) mbar_init(bar_o_free + 8 * b, 8);
         for (int u = 0; u < C::NU; ++u) {
             mbar_init(bar_u_full + 8 * u, 1);
-            mbar_init(bar_u_empty + 8 * u, 9 + C::NPROD);   // every role but the scheduler
+            mbar_init(bar_u_empty + 8 * u, 10 + C::NPK + C::NPV);   // every role but the scheduler
         }
         fence_barrier_init();
         *abort_flag = 0;
     }
-    if (warp == C::W_MMA) {
+    if (warp == C::W_MMA_S) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -297,80 +284,49 @@ __global__ void __launch_bounds__(512, 1)
                 if (q_last[b] >= 0)
                     mbar_drain(bar_q_full + 8 * b, (q_last[b] / C::NQB) & 1, kWaitLimitCycles / 8);
         }
-    } else if (warp >= 8 && warp < 8 + C::NPROD) {
+    } else if (warp >= 8 && warp < 8 + C::NPK + C::NPV) {
         // ============================================================ producers
-        // Sub-tile at ring position seq belongs to warp seq % 4: that warp alone
-        // waits for its slot, arms it with the sub-tile's bytes and issues its
-        // boxes (at most 16), one per lane, so the four warps load four
-        // sub-tiles at a time.
-        const int pw = warp - 8;
-        if (lane == 0 && pw == 0) {
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
-        }
+        // K warps fill the K ring, V warps the V ring.  Sub-tile sequence
+        // number seq of a ring belongs to warp seq % (warps of that ring):
+        // that warp alone waits for the slot, arms it with the sub-tile's
+        // bytes and issues its boxes (at most 16), one per lane.
+        const bool is_k = warp < 8 + C::NPK;
+        const int pw = is_k ? warp - 8 : warp - 8 - C::NPK;
+        const int nw = is_k ? C::NPK : C::NPV;
+        const int NS = is_k ? C::NKS : C::NVS;
+        const uint32_t full0 = is_k ? bar_kfull : bar_vfull;
+        const uint32_t empty0 = is_k ? bar_kempty : bar_vempty;
+        const uint32_t ring0 = is_k ? kring0 : vring0;
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        if (lane == 0 && pw == 0) prefetch_tensormap(map);
         pdl_wait();   // block tables and this step's K/V rows are written
         const int BR = a.box_rows;
         const uint64_t pol_keep = policy_evict_last();    // re-read by the request's other units
         const uint64_t pol_once = policy_evict_first();   // read by this unit alone
         uint64_t pol = pol_keep;
-        int seq = 0;        // ring position of the next sub-tile
+        int seq = 0;        // sequence number of the ring's next sub-tile
         bool bad = false;
-        // waits for the slot of position `seq` to be free and arms it with the
-        // sub-tile's bytes (arm = false only in the failure-path test); `bad`
-        // when the wait gave up
+        // waits for the slot of `seq` to be free and arms it with the sub-tile's
+        // bytes (arm = false only in the failure-path test); `bad` when the wait
+        // gave up
         auto acquire = [&](int bytes, bool arm) -> uint32_t {
-            const int slot = seq % C::NSLOT;
+            const int slot = seq % NS;
             if (lane == 0) {
-                if (seq >= C::NSLOT)
-                    bad = !mbar_wait(bar_empty + 8 * slot, ((seq / C::NSLOT) - 1) & 1, a.err,
-                                     abort_flag);
-                if (!bad && arm) mbar_arrive_expect_tx(bar_full + 8 * slot, bytes);
+                if (seq >= NS)
+                    bad = !mbar_wait(empty0 + 8 * slot, ((seq / NS) - 1) & 1, a.err, abort_flag);
+                if (!bad && arm) mbar_arrive_expect_tx(full0 + 8 * slot, bytes);
             }
             bad = __shfl_sync(0xffffffffu, (int)bad, 0);
             return (uint32_t)slot;
         };
-        // K sub-tile s (64-dim chunk s) of the tile starting at key kt with cnt
-        // keys, KV head h: one box per page run, lane u loads run u; pg: this
-        // lane's page id of page run `lane`
-        auto issue_k = [&](int s, int h, int kt, int cnt, int pg, bool skip) {
-            if (seq % C::NPROD == pw) {
-                const int nbox = (cnt + BR - 1) / BR;   // <= 16
-                const uint32_t slot = acquire(nbox * BR * 128, !skip);
-                if (!bad && !skip && lane < nbox)
-                    tma_load_3d(slot0 + slot * C::SLOT + lane * BR * 128, &kmap, s * 64, h,
-                                pg * bs + (kt + lane * BR) % bs, bar_full + 8 * slot, pol);
-            }
-            ++seq;
-        };
-        // V sub-tile s (keys [s VKEYS, (s + 1) VKEYS) of the tile, every
-        // 64-dim chunk: at most 16 boxes, lane b loads run u_lo + b / KCH,
-        // chunk b % KCH)
-        auto issue_v = [&](int s, int h, int kt, int cnt, int pg) {
-            const int runs = (cnt + BR - 1) / BR;
-            const int u_lo = s * (C::VKEYS / BR);
-            const int u_hi = min(runs, (s + 1) * (C::VKEYS / BR));
-            const int nbox = max(0, u_hi - u_lo) * C::KCH;
-            const int ul = lane / C::KCH, ch = lane % C::KCH;
-            const int u = u_lo + ul;
-            const int pgu = __shfl_sync(0xffffffffu, pg, u & 31);
-            if (seq % C::NPROD == pw) {
-                const uint32_t slot = acquire(nbox * BR * 128, true);
-                if (!bad && lane < nbox)
-                    tma_load_3d(slot0 + slot * C::SLOT + ch * (C::VKEYS * 128) + ul * BR * 128,
-                                &vmap, ch * 64, h, pgu * bs + (kt + u * BR) % bs,
-                                bar_full + 8 * slot, pol);
-            }
-            ++seq;
-        };
         // page id of page run `lane` of tile j of unit u (0 past the tile)
         auto load_pg = [&](const MqUnit &u, int j) -> int {
-            const int kt = tile_of(u, j) * C::BN;
+            const int kt = j * C::BN;
             const int runs = (min(C::BN, u.kend - kt) + BR - 1) / BR;
             return lane < runs ? __ldg(a.block_tables + (int64_t)u.r * a.max_blocks_per_seq +
                                        (kt + lane * BR) / bs)
                                : 0;
         };
-        int prev = 0, prev_h = 0, prev_kt = 0, prev_cnt = 0, prev_pg = 0;   // tile t - 1
         int t = 0;
         for (int k = 0; !bad; ++k) {
             MqUnit u;
@@ -383,90 +339,61 @@ __global__ void __launch_bounds__(512, 1)
             int pg_cur = load_pg(u, 0);
             int pg_nxt = u.ntiles > 1 ? load_pg(u, 1) : 0;
             for (int j = 0; j < u.ntiles && !bad; ++j) {
-                const int kt = tile_of(u, j) * C::BN;
+                const int kt = j * C::BN;
                 const int cnt = min(C::BN, u.kend - kt);
+                const int runs = (cnt + BR - 1) / BR;   // <= 16 page runs
                 // (failure-path test: the CTA's first K tile is neither armed
-                // nor loaded, so the MMA warp's bounded wait for it runs out)
-                const bool skip = t == 0 && a.test_skip_first_k;
-                if (C::PV_FIRST && j == 0 && prev) {   // unit boundary: V(t - 1), then K(t)
-                    for (int s = 0; s < C::SUB && !bad; ++s)
-                        issue_v(s, prev_h, prev_kt, prev_cnt, prev_pg);
-                    for (int s = 0; s < C::SUB && !bad; ++s)
-                        issue_k(s, u.h, kt, cnt, pg_cur, skip);
-                } else {
-                    for (int s = 0; s < C::SUB && !bad; ++s)
-                        issue_k(s, u.h, kt, cnt, pg_cur, skip);
-                    if (prev)
-                        for (int s = 0; s < C::SUB && !bad; ++s)
-                            issue_v(s, prev_h, prev_kt, prev_cnt, prev_pg);
+                // nor loaded, so the S issuer's bounded wait for it runs out)
+                const bool skip = is_k && t == 0 && a.test_skip_first_k;
+#pragma unroll 1
+                for (int s = 0; s < C::SUB && !bad; ++s, ++seq) {
+                    if (is_k) {
+                        // K sub-tile s: 64-dim chunk s of the tile's keys, one box
+                        // per page run, lane u loads run u
+                        if (seq % nw == pw) {
+                            const uint32_t slot = acquire(runs * BR * 128, !skip);
+                            if (!bad && !skip && lane < runs)
+                                tma_load_3d(ring0 + slot * C::SLOT + lane * BR * 128, map, s * 64,
+                                            u.h, pg_cur * bs + (kt + lane * BR) % bs,
+                                            full0 + 8 * slot, pol);
+                        }
+                    } else {
+                        // V sub-tile s: keys [s VKEYS, (s + 1) VKEYS) of every 64-dim
+                        // chunk; lane b loads run u_lo + b / KCH, chunk b % KCH
+                        const int u_lo = s * (C::VKEYS / BR);
+                        const int u_hi = min(runs, (s + 1) * (C::VKEYS / BR));
+                        const int nbox = max(0, u_hi - u_lo) * C::KCH;
+                        const int ul = lane / C::KCH, ch = lane % C::KCH;
+                        const int ru = u_lo + ul;
+                        const int pgu = __shfl_sync(0xffffffffu, pg_cur, ru & 31);
+                        if (seq % nw == pw) {
+                            const uint32_t slot = acquire(nbox * BR * 128, true);
+                            if (!bad && lane < nbox)
+                                tma_load_3d(ring0 + slot * C::SLOT + ch * (C::VKEYS * 128) +
+                                                ul * BR * 128,
+                                            map, ch * 64, u.h, pgu * bs + (kt + ru * BR) % bs,
+                                            full0 + 8 * slot, pol);
+                        }
+                    }
                 }
-                prev = 1;
-                prev_h = u.h;
-                prev_kt = kt;
-                prev_cnt = cnt;
-                prev_pg = pg_cur;
                 pg_cur = pg_nxt;
                 if (j + 2 < u.ntiles) pg_nxt = load_pg(u, j + 2);
                 ++t;
             }
         }
-        // after the last tile its V, preceded when !PV_FIRST by an empty K (no
-        // boxes: the slot completes on its owner's arrival alone)
-        if (prev && !bad) {
-            if (!C::PV_FIRST)
-                for (int s = 0; s < C::SUB && !bad; ++s) issue_k(s, 0, 0, 0, 0, false);
-            for (int s = 0; s < C::SUB && !bad; ++s) issue_v(s, prev_h, prev_kt, prev_cnt, prev_pg);
-        }
         // copies in flight land before the CTA can exit (bounded)
         if (lane == 0)
-            for (int i = max(0, seq - C::NSLOT); i < seq; ++i)
-                mbar_drain(bar_full + 8 * (i % C::NSLOT), (i / C::NSLOT) & 1, kWaitLimitCycles / 8);
-    } else if (warp == C::W_MMA) {
-        // ============================================================ MMA issuer
+            for (int i = max(0, seq - NS); i < seq; ++i)
+                mbar_drain(full0 + 8 * (i % NS), (i / NS) & 1, kWaitLimitCycles / 8);
+    } else if (warp == C::W_MMA_S) {
+        // ============================================================ S issuer
+        // S(t) = Q K(t)^T into TMEM buffer t % NSB, once PV(t - NSB) has read P(t - NSB)
+        // out of it; K sub-tiles are freed in the order they were filled.
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, C::BN, 0, 0);
-            constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
             int t = 0, itn = 0;
             uint32_t last_commit = 0, last_parity = 0;   // drained before TMEM is freed
             bool any = false;
-            // the PV of tile tp (cnt keys) into accumulator ob; first / last: the
-            // unit's first (overwrite O) / last tile; itn_p: the unit's number
-            auto issue_pv = [&](int tp, int cnt, int ob, bool first, bool last, int itn_p) {
-                if (first && itn_p >= C::NOB)   // the unit NOB back has read its O out
-                    mbar_wait(bar_o_free + 8 * ob, ((itn_p / C::NOB) - 1) & 1, a.err, abort_flag);
-                mbar_wait(bar_p_full + 8 * (tp & 1), (tp >> 1) & 1, a.err, abort_flag);
-                const int p0 = mq_pos_v(tp, C::SUB, C::PV_FIRST, last);
-                const int nk = (cnt + 15) / 16;   // 16-key steps holding keys
-                const uint32_t pt = tmem + (tp & 1) * C::BN;
-                constexpr int KPS = C::VKEYS / 16;   // steps per V sub-tile
-#pragma unroll
-                for (int s = 0; s < C::SUB; ++s) {
-                    const int slot = (p0 + s) % C::NSLOT;
-                    mbar_wait(bar_full + 8 * slot, ((p0 + s) / C::NSLOT) & 1, a.err, abort_flag);
-                    tc_fence_after();
-                    const uint32_t vs = slot0 + slot * C::SLOT;
-#pragma unroll
-                    for (int kl = 0; kl < KPS; ++kl) {
-                        const int kk = s * KPS + kl;
-                        if (kk >= nk) break;
-                        // V as MN-major B: atoms of 64 dims x 8 keys; LBO steps
-                        // the 64-dim chunks, SBO the 8-key groups
-                        const uint64_t bd =
-                            smem_desc_sw128(vs + kl * 16 * 128, C::VKEYS * 128, 1024);
-                        // P of keys [16 kk, 16 kk + 16): warpgroup kk / 4's columns
-                        const uint32_t pa = pt + 64 * (kk >> 2) + (kk & 3) * 8;
-                        tc_mma_bf16_ts(tmem + C::O_COL + ob * D, pa, bd, IDESC_O,
-                                       (first && kk == 0) ? 0u : 1u);
-                    }
-                    tc_commit(bar_empty + 8 * slot);   // this sub-tile's MMAs done
-                }
-                tc_commit(bar_o_done + 8 * (tp & 1));
-                last_commit = bar_o_done + 8 * (tp & 1);
-                last_parity = (tp >> 1) & 1;
-                any = true;
-            };
-            bool pv_pending = false, pv_first = false, pv_last = false;
-            int pv_t = 0, pv_cnt = 0, pv_ob = 0, pv_itn = 0;
             for (int k = 0;; ++k) {
                 MqUnit u;
                 const bool ok = take_unit(k, u);
@@ -474,28 +401,22 @@ __global__ void __launch_bounds__(512, 1)
                 if (!ok || u.r < 0 || *abort_flag) break;
                 if (u.ntiles == 0) continue;
                 const int qb = itn % C::NQB;
-                const int ob = itn % C::NOB;
-                // one Q buffer: the previous unit's last PV goes first (its
-                // epilogue need not wait for this unit's Q load); the order is
-                // fixed, as the ring's (mq_pos_k)
-                if (C::PV_FIRST && pv_pending) {
-                    issue_pv(pv_t, pv_cnt, pv_ob, pv_first, pv_last, pv_itn);
-                    pv_pending = false;
-                }
                 mbar_wait(bar_q_full + 8 * qb, (itn / C::NQB) & 1, a.err, abort_flag);
                 const uint32_t qs = q_smem + qb * C::Q_BYTES;
                 for (int j = 0; j < u.ntiles; ++j) {
-                    const int sb = t & 1;
-                    // S(t) = Q K(t)^T into buffer sb (its last reader, PV(t - 2),
-                    // was issued before by this thread)
-                    const int p0 = mq_pos_k(t, C::SUB, C::PV_FIRST, j == 0);
+                    const int sb = t % C::NSB;
+                    if (t >= C::NSB)   // PV(t - NSB) has read P(t - NSB) out of buffer sb
+                        mbar_wait(bar_o_done + 8 * sb, ((t - C::NSB) / C::NSB) & 1, a.err,
+                                  abort_flag);
+                    const int p0 = t * C::SUB;
+#pragma unroll
+                    for (int s = 0; s < C::SUB; ++s)
+                        mbar_wait(bar_kfull + 8 * ((p0 + s) % C::NKS), ((p0 + s) / C::NKS) & 1,
+                                  a.err, abort_flag);
+                    tc_fence_after();
 #pragma unroll
                     for (int s = 0; s < C::SUB; ++s) {   // 64-dim chunk s of K and Q
-                        const int slot = (p0 + s) % C::NSLOT;
-                        mbar_wait(bar_full + 8 * slot, ((p0 + s) / C::NSLOT) & 1, a.err,
-                                  abort_flag);
-                        tc_fence_after();
-                        const uint32_t ks = slot0 + slot * C::SLOT;
+                        const uint32_t ks = kring0 + ((p0 + s) % C::NKS) * C::SLOT;
 #pragma unroll
                         for (int kl = 0; kl < 4; ++kl) {
                             const uint32_t off = kl * 32;   // 16 bf16 within the 128-B row
@@ -505,37 +426,82 @@ __global__ void __launch_bounds__(512, 1)
                             tc_mma_bf16(tmem + sb * C::BN, ad, bd, IDESC_S,
                                         (s > 0 || kl > 0) ? 1u : 0u);
                         }
-                        tc_commit(bar_empty + 8 * slot);   // this chunk's MMAs done
                     }
+#pragma unroll
+                    for (int s = 0; s < C::SUB; ++s)
+                        tc_commit(bar_kempty + 8 * ((p0 + s) % C::NKS));
                     tc_commit(bar_s_full + 8 * sb);
+                    last_commit = bar_s_full + 8 * sb;
+                    last_parity = (t / C::NSB) & 1;
+                    any = true;
                     if (j == u.ntiles - 1) tc_commit(bar_q_empty + 8 * qb);
-                    if (pv_pending) issue_pv(pv_t, pv_cnt, pv_ob, pv_first, pv_last, pv_itn);
-                    pv_pending = true;
-                    pv_t = t;
-                    pv_cnt = min(C::BN, u.kend - tile_of(u, j) * C::BN);
-                    pv_ob = ob;
-                    pv_first = j == 0;
-                    pv_last = j == u.ntiles - 1;
-                    pv_itn = itn;
                     ++t;
                 }
                 ++itn;
             }
-            if (pv_pending) {
-                if (!C::PV_FIRST) {
-                    // the producers' empty K after the last tile: release its slots
-                    const int p0 = mq_pos_k(t, C::SUB, false, false);
-#pragma unroll
-                    for (int s = 0; s < C::SUB; ++s) {
-                        mbar_wait(bar_full + 8 * ((p0 + s) % C::NSLOT),
-                                  ((p0 + s) / C::NSLOT) & 1, a.err, abort_flag);
-                        mbar_arrive(bar_empty + 8 * ((p0 + s) % C::NSLOT));
-                    }
-                }
-                issue_pv(pv_t, pv_cnt, pv_ob, pv_first, pv_last, pv_itn);
-            }
             // every MMA is finished before TMEM is freed (bounded, also when
             // the pipeline was aborted)
+            if (any) mbar_drain(last_commit, last_parity, kWaitLimitCycles / 8);
+        }
+    } else if (warp == C::W_MMA_PV) {
+        // ============================================================ PV issuer
+        // O += P(t) V(t) once the softmax has written P(t); V sub-tiles are
+        // freed in the order they were filled.
+        if (lane == 0) {
+            constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
+            constexpr int KPS = C::VKEYS / 16;   // 16-key steps per V sub-tile
+            int t = 0, itn = 0;
+            uint32_t last_commit = 0, last_parity = 0;
+            bool any = false;
+            for (int k = 0;; ++k) {
+                MqUnit u;
+                const bool ok = take_unit(k, u);
+                mbar_arrive(bar_u_empty + 8 * (k % C::NU));
+                if (!ok || u.r < 0 || *abort_flag) break;
+                if (u.ntiles == 0) continue;
+                const int ob = itn % C::NOB;
+                const uint32_t od = tmem + C::O_COL + ob * D;
+                for (int j = 0; j < u.ntiles; ++j) {
+                    if (j == 0 && itn >= C::NOB)   // the unit NOB back has read its O out
+                        mbar_wait(bar_o_free + 8 * ob, ((itn / C::NOB) - 1) & 1, a.err,
+                                  abort_flag);
+                    mbar_wait(bar_p_full + 8 * (t % C::NSB), (t / C::NSB) & 1, a.err, abort_flag);
+                    const int cnt = min(C::BN, u.kend - j * C::BN);
+                    const int nk = (cnt + 15) / 16;   // 16-key steps holding keys
+                    const int p0 = t * C::SUB;
+#pragma unroll
+                    for (int s = 0; s < C::SUB; ++s)
+                        mbar_wait(bar_vfull + 8 * ((p0 + s) % C::NVS), ((p0 + s) / C::NVS) & 1,
+                                  a.err, abort_flag);
+                    tc_fence_after();
+                    const uint32_t pt = tmem + (t % C::NSB) * C::BN;
+#pragma unroll
+                    for (int s = 0; s < C::SUB; ++s) {
+                        const uint32_t vs = vring0 + ((p0 + s) % C::NVS) * C::SLOT;
+#pragma unroll
+                        for (int kl = 0; kl < KPS; ++kl) {
+                            const int kk = s * KPS + kl;
+                            if (kk >= nk) break;
+                            // V as MN-major B: atoms of 64 dims x 8 keys; LBO steps
+                            // the 64-dim chunks, SBO the 8-key groups
+                            const uint64_t bd =
+                                smem_desc_sw128(vs + kl * 16 * 128, C::VKEYS * 128, 1024);
+                            // P of keys [16 kk, 16 kk + 16): warpgroup kk / 4's columns
+                            const uint32_t pa = pt + 64 * (kk >> 2) + (kk & 3) * 8;
+                            tc_mma_bf16_ts(od, pa, bd, IDESC_O, (j == 0 && kk == 0) ? 0u : 1u);
+                        }
+                    }
+#pragma unroll
+                    for (int s = 0; s < C::SUB; ++s)
+                        tc_commit(bar_vempty + 8 * ((p0 + s) % C::NVS));
+                    tc_commit(bar_o_done + 8 * (t % C::NSB));
+                    last_commit = bar_o_done + 8 * (t % C::NSB);
+                    last_parity = (t / C::NSB) & 1;
+                    any = true;
+                    ++t;
+                }
+                ++itn;
+            }
             if (any) mbar_drain(last_commit, last_parity, kWaitLimitCycles / 8);
         }
     } else {
@@ -575,8 +541,8 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t o_lane = t_lane + C::O_COL + ob * D + wg * (D / 2);
             float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;   // l: this half's sum
             for (int j = 0; j < u.ntiles; ++j) {
-                const int sb = t & 1;
-                mbar_wait(bar_s_full + 8 * sb, (t >> 1) & 1, a.err, abort_flag);
+                const int sb = t % C::NSB;
+                mbar_wait(bar_s_full + 8 * sb, (t / C::NSB) & 1, a.err, abort_flag);
                 tc_fence_after();
                 float s[HB];
                 tmem_ld32(t_lane + sb * C::BN + kb, s);
@@ -619,20 +585,19 @@ __global__ void __launch_bounds__(512, 1)
                 const int cnt = min(C::BN, u.kend - kt0);
                 if (cnt & 15) {
                     const int s_v = cnt / C::VKEYS;                  // V sub-tile holding them
-                    const int pos = mq_pos_v(t, C::SUB, C::PV_FIRST, j == u.ntiles - 1) + s_v;
-                    // A parity wait is only meaningful while the barrier is at most
-                    // one phase away.  Once S(t) is done every MMA before it is done
-                    // too, so the slot's previous use is complete -- unless it is
-                    // the V of tile t - 1, whose PV may still run: wait for that PV
-                    // first.  (With the ring sizes used, the previous use is never
-                    // that V; the wait keeps the rule true for any size.)
-                    const int pv1 = t >= 1 ? mq_pos_v(t - 1, C::SUB, C::PV_FIRST, j == 0) : 0;
-                    if (t >= 1 && pos - C::NSLOT >= pv1 && pos - C::NSLOT < pv1 + C::SUB)
-                        mbar_wait(bar_o_done + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, a.err,
+                    const int pos = t * C::SUB + s_v;                // its V ring sequence number
+                    // A parity wait tells the phase of `pos` from that of pos - NVS
+                    // only once the latter has completed.  If pos - NVS belongs to a
+                    // tile tp > t - NSB, PV(tp) may not even have started: wait for
+                    // it.  Older sub-tiles were read by PV(t - NSB) or earlier, which
+                    // finished before S(t) was issued.
+                    const int tp = pos >= C::NVS ? (pos - C::NVS) / C::SUB : -1;
+                    if (tp >= 0 && tp > t - C::NSB)
+                        mbar_wait(bar_o_done + 8 * (tp % C::NSB), (tp / C::NSB) & 1, a.err,
                                   abort_flag);
-                    mbar_wait(bar_full + 8 * (pos % C::NSLOT), (pos / C::NSLOT) & 1, a.err,
+                    mbar_wait(bar_vfull + 8 * (pos % C::NVS), (pos / C::NVS) & 1, a.err,
                               abort_flag);
-                    uint8_t *vsp = smem + C::OFF_SLOT + (pos % C::NSLOT) * C::SLOT;
+                    uint8_t *vsp = smem + C::OFF_VSLOT + (pos % C::NVS) * C::SLOT;
                     const int k0 = cnt - s_v * C::VKEYS;             // first row to clear
                     const int nclr = 16 - (cnt & 15);
                     for (int q = wg * 128 + m; q < nclr * C::KCH * 8; q += 256) {
@@ -645,7 +610,7 @@ __global__ void __launch_bounds__(512, 1)
                 // O changes only when a row's reference max moves: then PV(t - 1)
                 // of this unit must be done.  Each warpgroup rescales its half.
                 if (j >= 1 && __any_sync(0xffffffffu, need)) {
-                    mbar_wait(bar_o_done + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, a.err,
+                    mbar_wait(bar_o_done + 8 * ((t - 1) % C::NSB), ((t - 1) / C::NSB) & 1, a.err,
                               abort_flag);
                     tc_fence_after();
                     const float f = need ? (m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new)) : 1.f;
@@ -699,7 +664,8 @@ __global__ void __launch_bounds__(512, 1)
             }
             // ---- epilogue: out = O / (l + sink term); each warpgroup writes half of D
             if (u.ntiles > 0) {
-                mbar_wait(bar_o_done + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, a.err, abort_flag);
+                mbar_wait(bar_o_done + 8 * ((t - 1) % C::NSB), ((t - 1) / C::NSB) & 1, a.err,
+                          abort_flag);
                 tc_fence_after();
             }
             const float l_row = l + exchange(l);
@@ -751,7 +717,7 @@ __global__ void __launch_bounds__(512, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == C::W_MMA) {
+    if (warp == C::W_MMA_S) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }

@@ -6,22 +6,24 @@ The kernel's roles meet only through mbarriers whose waits test a phase
 *parity*: a wait for phase k passes as soon as the barrier's current phase
 has the other parity, so it cannot tell phase k from phase k - 2.  Whether
 every wait is at most one phase away depends on the order in which the roles
-fill and free the shared-memory ring of K/V sub-tiles, the unit ring, the Q
-buffers, the S/P and O regions of TMEM.  This model replays that order with
-the same position arithmetic as the kernel (ring positions of K(t) and V(t),
-one or two Q buffers and O accumulators by head_dim, NPROD producer warps
-taking positions round robin) and checks, for every interleaving it draws:
+fill and free the shared-memory rings of K and V sub-tiles, the unit ring,
+the Q buffers, and the S/P and O regions of TMEM.  This model replays that
+order with the kernel's arithmetic -- a K ring and a V ring of 16 KB
+sub-tiles filled round robin by their producer warps, an S issuer and a PV
+issuer (each frees its ring in fill order), NSB S/P buffers and NOB O
+accumulators by head_dim, the softmax's zeroing of value rows past a tile's
+last key -- and checks, for every interleaving it draws:
 
 * no parity wait passes while the phase it waits for is still open;
 * a slot is re-armed only after every MMA reading it has finished;
-* every MMA reads a slot (or Q buffer) holding the position it expects, landed;
-* O is not overwritten during its epilogue, and S(t + 2) does not overwrite
-  S(t) before the softmax has read it.
+* every MMA reads a slot (or Q buffer) holding the sub-tile it expects, landed;
+* S(t) does not overwrite P(t - NSB) before PV(t - NSB) has read it, and O is
+  not overwritten during its epilogue.
 
 The tensor pipe completes MMAs and commits in issue order; TMA copies land in
-any order.  It also shows that the model has teeth: with the claim order of
-an earlier version (the previous unit's last PV issued before the new unit's
-first S only when the new Q had not landed yet) it finds a stale parity pass.
+any order.  Two planted mistakes show that the model has teeth: dropping the
+S issuer's wait for PV(t - NSB), and dropping the softmax's wait for the PV
+that last read the slot it zeroes.
 """
 import random
 from collections import deque
@@ -75,50 +77,43 @@ def units_of(lengths, D, G, prior=None, causal=True):
     return out
 
 
-def simulate(D, units, nprod, seed, order="fixed"):
+def simulate(D, units, kp, vp, seed, mutate=None):
+    """One random interleaving of the kernel's roles over `units` (kp K and vp
+    V producer warps); raises AssertionError on a violation."""
     rnd = random.Random(seed)
     SUB = D // 64
-    NSLOT = 10 if D >= 128 else 12
+    NR = 5 if D >= 128 else 6            # slots per ring
     NQB = 1 if D >= 256 else 2
-    NOB = 1 if D >= 256 else 2
+    NSB = 2 if D >= 256 else 3           # S/P buffers in TMEM
+    NOB = 2 if D <= 64 else 1
     NU, BN = 8, 128
     VKEYS = BN // SUB
-    PV_FIRST = NQB == 1
-
-    def pos_k(t, unit_first):
-        if t == 0:
-            return 0
-        return (2 * t - 1) * SUB + (SUB if (PV_FIRST and unit_first and order == "fixed") else 0)
-
-    def pos_v(t, unit_last):
-        if PV_FIRST and order == "fixed":
-            return (2 * t + 1) * SUB + (0 if unit_last else SUB)
-        return (2 * t + 2) * SUB
-
-    B = lambda name, n, c: [Bar(f"{name}{i}", c) for i in range(n)]  # noqa: E731
+    B = lambda n, k, c: [Bar(f"{n}{i}", c) for i in range(k)]  # noqa: E731
     q_full, q_empty = B("q_full", NQB, 1), B("q_empty", NQB, 1)
-    full, empty = B("full", NSLOT, 1), B("empty", NSLOT, 1)
-    s_full, p_full, o_done = B("s_full", 2, 1), B("p_full", 2, 1), B("o_done", 2, 1)
+    kfull, kempty = B("kfull", NR, 1), B("kempty", NR, 1)
+    vfull, vempty = B("vfull", NR, 1), B("vempty", NR, 1)
+    s_full, p_full, o_done = B("s_full", NSB, 1), B("p_full", NSB, 1), B("o_done", NSB, 1)
     o_free = B("o_free", NOB, 1)
-    u_full, u_empty = B("u_full", NU, 1), B("u_empty", NU, nprod + 2)
+    u_full, u_empty = B("u_full", NU, 1), B("u_empty", NU, 1 + kp + vp + 2)
     ring = [None] * NU
-    slot_pos, slot_landed, slot_readers = [None] * NSLOT, [False] * NSLOT, [0] * NSLOT
+    kslot = {"pos": [None] * NR, "landed": [False] * NR, "readers": [0] * NR}
+    vslot = {"pos": [None] * NR, "landed": [False] * NR, "readers": [0] * NR}
     q_unit, q_landed, q_readers = [None] * NQB, [False] * NQB, [0] * NQB
-    o_epilogue = [False] * NOB
+    o_epi = [False] * NOB
+    s_buf_readers = [0] * 3   # PV MMAs in flight reading P from S buffer b
     copies, pipe = [], deque()
-    s_read, p_written = set(), set()
+    state = {"s_read": set(), "p_written": set(), "s_written": set()}
 
     def wait(bar, parity, phase):
         while not bar.try_wait(parity):
             yield
         if bar.phase <= phase:
-            raise StaleWait(f"{bar.name}: parity wait for phase {phase} passed with "
-                            f"{bar.phase} phases complete")
+            raise StaleWait(f"{bar.name}: wait for phase {phase} passed at {bar.phase}")
 
     def take(k):
         yield from wait(u_full[k % NU], (k // NU) & 1, k // NU)
         kk, u = ring[k % NU]
-        assert kk == k, "unit ring entry overwritten before it was read"
+        assert kk == k
         return u
 
     def scheduler():
@@ -135,32 +130,17 @@ def simulate(D, units, nprod, seed, order="fixed"):
                 qb = itn % NQB
                 if itn >= NQB:
                     yield from wait(q_empty[qb], (itn // NQB - 1) & 1, itn // NQB - 1)
-                assert not q_readers[qb], "Q buffer reloaded while MMAs read it"
+                assert not q_readers[qb], "Q reloaded while read"
                 q_unit[qb], q_landed[qb] = itn, False
                 q_full[qb].arrive(tx=1)
                 copies.append((q_full[qb], "q", qb))
                 itn += 1
             yield
 
-    def producer(pw):
+    def producer(which, pw, nw):
+        full, empty, sl = (kfull, kempty, kslot) if which == "k" else (vfull, vempty, vslot)
         seq = 0
-
-        def group(nbytes):
-            nonlocal seq
-            for _ in range(SUB):
-                if seq % nprod == pw:
-                    s = seq % NSLOT
-                    if seq >= NSLOT:
-                        yield from wait(empty[s], (seq // NSLOT - 1) & 1, seq // NSLOT - 1)
-                    assert not slot_readers[s], f"slot {s} re-armed while an MMA reads it"
-                    slot_pos[s], slot_landed[s] = seq, nbytes == 0
-                    full[s].arrive(tx=nbytes)
-                    if nbytes:
-                        copies.append((full[s], "kv", s))
-                seq += 1
-                yield
-
-        prev, k = False, 0
+        k = 0
         while True:
             u = yield from take(k)
             u_empty[k % NU].arrive()
@@ -168,48 +148,27 @@ def simulate(D, units, nprod, seed, order="fixed"):
             if u is None:
                 break
             for j in range(u["ntiles"]):
-                if PV_FIRST and order == "fixed" and j == 0 and prev:
-                    yield from group(1)          # V(t - 1)
-                    yield from group(1)          # K(t)
-                else:
-                    yield from group(1)          # K(t)
-                    if prev:
-                        yield from group(1)      # V(t - 1)
-                prev = True
-        if prev:
-            if not (PV_FIRST and order == "fixed"):
-                yield from group(0)              # empty K
-            yield from group(1)                  # V(last)
+                for s in range(SUB):
+                    if seq % nw == pw:
+                        slot = seq % NR
+                        if seq >= NR:
+                            yield from wait(empty[slot], (seq // NR - 1) & 1, seq // NR - 1)
+                        assert not sl["readers"][slot], f"{which} slot {slot} re-armed while read"
+                        if which == "v" and zeroing[0] == slot:
+                            raise AssertionError("V slot re-armed during zeroing")
+                        sl["pos"][slot], sl["landed"][slot] = seq, False
+                        full[slot].arrive(tx=1)
+                        copies.append((full[slot], which, slot))
+                    seq += 1
+                    yield
 
-    def mma_read(reads, q=None):
-        for s, p in reads:
-            assert slot_pos[s] == p and slot_landed[s], \
-                f"MMA reads slot {s} for position {p}: holds {slot_pos[s]}"
-            slot_readers[s] += 1
-        if q is not None:
-            assert q_landed[q[0]] and q_unit[q[0]] == q[1], "MMA reads a Q not landed"
-            q_readers[q[0]] += 1
-        pipe.append(("mma", reads, q))
+    def read(sl, slot, pos, tag):
+        assert sl["pos"][slot] == pos and sl["landed"][slot], \
+            f"{tag}: slot {slot} holds {sl['pos'][slot]}, wants {pos}"
+        sl["readers"][slot] += 1
 
-    def mma():
+    def mma_s():
         t = itn = k = 0
-        pv = None
-
-        def issue_pv(tp, cnt, ob, first, last, itn_p):
-            if first and itn_p >= NOB:
-                yield from wait(o_free[ob], (itn_p // NOB - 1) & 1, itn_p // NOB - 1)
-                assert not o_epilogue[ob], "O overwritten during its epilogue"
-            yield from wait(p_full[tp & 1], (tp >> 1) & 1, tp >> 1)
-            assert tp in p_written
-            p0 = pos_v(tp, last)
-            for s in range(SUB):
-                sl = (p0 + s) % NSLOT
-                yield from wait(full[sl], ((p0 + s) // NSLOT) & 1, (p0 + s) // NSLOT)
-                if s * (VKEYS // 16) < (cnt + 15) // 16:
-                    mma_read([(sl, p0 + s)])
-                pipe.append(("commit", empty[sl]))
-            pipe.append(("commit", o_done[tp & 1]))
-
         while True:
             u = yield from take(k)
             u_empty[k % NU].arrive()
@@ -218,37 +177,74 @@ def simulate(D, units, nprod, seed, order="fixed"):
                 break
             if not u["ntiles"]:
                 continue
-            qb, ob = itn % NQB, itn % NOB
-            if pv is not None and PV_FIRST and (
-                    order == "fixed" or not q_full[qb].try_wait((itn // NQB) & 1)):
-                yield from issue_pv(*pv)
-                pv = None
+            qb = itn % NQB
             yield from wait(q_full[qb], (itn // NQB) & 1, itn // NQB)
             for j in range(u["ntiles"]):
-                assert t < 2 or (t - 2) in s_read, "S overwritten before the softmax read it"
-                p0 = pos_k(t, j == 0)
+                b = t % NSB
+                if t >= NSB and mutate != "no_sbuf_wait":
+                    yield from wait(o_done[b], ((t - NSB) // NSB) & 1, (t - NSB) // NSB)
+                if s_buf_readers[b]:
+                    raise AssertionError(f"S({t}) overwrites P({t-NSB}) still read by PV")
+                assert t < NSB or (t - NSB) in state["s_read"]
+                reads = []
                 for s in range(SUB):
-                    sl = (p0 + s) % NSLOT
-                    yield from wait(full[sl], ((p0 + s) // NSLOT) & 1, (p0 + s) // NSLOT)
-                    mma_read([(sl, p0 + s)], (qb, itn))
-                    pipe.append(("commit", empty[sl]))
-                pipe.append(("commit", s_full[t & 1]))
+                    p = t * SUB + s
+                    slot = p % NR
+                    yield from wait(kfull[slot], (p // NR) & 1, p // NR)
+                for s in range(SUB):
+                    p = t * SUB + s
+                    read(kslot, p % NR, p, "S")
+                    reads.append(("k", p % NR))
+                assert q_landed[qb] and q_unit[qb] == itn
+                q_readers[qb] += 1
+                pipe.append(("mma", reads, ("q", qb), ("sw", b, t)))
+                for s in range(SUB):
+                    pipe.append(("commit", kempty[(t * SUB + s) % NR]))
+                pipe.append(("commit", s_full[b]))
                 if j == u["ntiles"] - 1:
                     pipe.append(("commit", q_empty[qb]))
-                if pv is not None:
-                    yield from issue_pv(*pv)
-                pv = (t, min(BN, u["kend"] - j * BN), ob, j == 0, j == u["ntiles"] - 1, itn)
                 t += 1
                 yield
             itn += 1
-        if pv is not None:
-            if not (PV_FIRST and order == "fixed"):
-                p0 = pos_k(t, False)
+
+    def mma_pv():
+        t = itn = k = 0
+        while True:
+            u = yield from take(k)
+            u_empty[k % NU].arrive()
+            k += 1
+            if u is None:
+                break
+            if not u["ntiles"]:
+                continue
+            ob = itn % NOB
+            for j in range(u["ntiles"]):
+                if j == 0 and itn >= NOB:
+                    yield from wait(o_free[ob], (itn // NOB - 1) & 1, itn // NOB - 1)
+                    assert not o_epi[ob], "O overwritten during its epilogue"
+                yield from wait(p_full[t % NSB], (t // NSB) & 1, t // NSB)
+                assert t in state["p_written"]
+                cnt = min(BN, u["kend"] - j * BN)
+                nk = (cnt + 15) // 16
                 for s in range(SUB):
-                    sl = (p0 + s) % NSLOT
-                    yield from wait(full[sl], ((p0 + s) // NSLOT) & 1, (p0 + s) // NSLOT)
-                    empty[sl].arrive()
-            yield from issue_pv(*pv)
+                    p = t * SUB + s
+                    yield from wait(vfull[p % NR], (p // NR) & 1, p // NR)
+                reads = []
+                for s in range(SUB):
+                    p = t * SUB + s
+                    if s * (VKEYS // 16) < nk:
+                        read(vslot, p % NR, p, "PV")
+                        reads.append(("v", p % NR))
+                s_buf_readers[t % NSB] += 1
+                pipe.append(("mma", reads, None, ("pr", t % NSB, t)))
+                for s in range(SUB):
+                    pipe.append(("commit", vempty[(t * SUB + s) % NR]))
+                pipe.append(("commit", o_done[t % NSB]))
+                t += 1
+                yield
+            itn += 1
+
+    zeroing = [None]
 
     def softmax():
         t = itn = k = 0
@@ -259,30 +255,38 @@ def simulate(D, units, nprod, seed, order="fixed"):
             if u is None:
                 break
             for j in range(u["ntiles"]):
-                yield from wait(s_full[t & 1], (t >> 1) & 1, t >> 1)
-                s_read.add(t)
+                yield from wait(s_full[t % NSB], (t // NSB) & 1, t // NSB)
+                assert t in state["s_written"]
+                state["s_read"].add(t)
                 cnt = min(BN, u["kend"] - j * BN)
-                if cnt & 15:   # zero the value rows past the last key in the slot
-                    pos = pos_v(t, j == u["ntiles"] - 1) + cnt // VKEYS
-                    pv1 = pos_v(t - 1, j == 0) if t else 0
-                    if t and pv1 <= pos - NSLOT < pv1 + SUB:
-                        yield from wait(o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, (t - 1) >> 1)
-                    sl = pos % NSLOT
-                    yield from wait(full[sl], (pos // NSLOT) & 1, pos // NSLOT)
-                    assert slot_pos[sl] == pos and slot_landed[sl] and not slot_readers[sl]
-                p_written.add(t)
-                p_full[t & 1].arrive()
+                if cnt & 15:
+                    pos = t * SUB + cnt // VKEYS
+                    prev = pos - NR
+                    tp = prev // SUB if prev >= 0 else -1   # tile of the slot's previous sub-tile
+                    if tp >= 0 and tp > t - NSB and mutate != "no_vtail_wait":
+                        yield from wait(o_done[tp % NSB], (tp // NSB) & 1, tp // NSB)
+                    slot = pos % NR
+                    yield from wait(vfull[slot], (pos // NR) & 1, pos // NR)
+                    assert vslot["pos"][slot] == pos and vslot["landed"][slot] \
+                        and not vslot["readers"][slot], "V-tail zeroing on a wrong or busy slot"
+                    zeroing[0] = slot
+                    yield
+                    zeroing[0] = None
+                state["p_written"].add(t)
+                p_full[t % NSB].arrive()
                 t += 1
                 yield
             if u["ntiles"]:
-                yield from wait(o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, (t - 1) >> 1)
-                o_epilogue[itn % NOB] = True
+                yield from wait(o_done[(t - 1) % NSB], ((t - 1) // NSB) & 1, (t - 1) // NSB)
+                ob = itn % NOB
+                o_epi[ob] = True
                 yield
-                o_epilogue[itn % NOB] = False
-                o_free[itn % NOB].arrive()
+                o_epi[ob] = False
+                o_free[ob].arrive()
                 itn += 1
 
-    roles = [scheduler(), mma(), softmax()] + [producer(pw) for pw in range(nprod)]
+    roles = [scheduler(), mma_s(), mma_pv(), softmax()]
+    roles += [producer("k", i, kp) for i in range(kp)] + [producer("v", i, vp) for i in range(vp)]
     alive = list(range(len(roles)))
     for _ in range(3_000_000):
         if not (alive or copies or pipe):
@@ -295,18 +299,24 @@ def simulate(D, units, nprod, seed, order="fixed"):
                 alive.remove(alive[c])
         elif copies and c == len(alive):
             bar, kind, i = copies.pop(rnd.randrange(len(copies)))
-            (q_landed if kind == "q" else slot_landed)[i] = True
+            {"q": q_landed, "k": kslot["landed"], "v": vslot["landed"]}[kind][i] = True
             bar.complete_tx(1)
         else:
+            # the tensor pipe executes in order; two issuers' MMAs interleave in the pipe
             item = pipe.popleft()
             if item[0] == "commit":
                 item[1].arrive()
             else:
-                for s, _ in item[1]:
-                    slot_readers[s] -= 1
-                if item[2] is not None:
-                    q_readers[item[2][0]] -= 1
-    raise AssertionError("no progress: the protocol deadlocked")
+                for which, slot in item[1]:
+                    (kslot if which == "k" else vslot)["readers"][slot] -= 1
+                if item[2]:
+                    q_readers[item[2][1]] -= 1
+                tag = item[3]
+                if tag[0] == "sw":
+                    state["s_written"].add(tag[2])
+                if tag[0] == "pr":
+                    s_buf_readers[tag[1]] -= 1
+    raise AssertionError("deadlock")
 
 
 CASES = {
@@ -316,31 +326,28 @@ CASES = {
     # prefill chunks and verify windows over prior context at head_dim 128
     "mixed-D128": (128, units_of([512, 512, 3, 5, 2], 128, 4, prior=[900, 1500, 800, 300, 2000])),
     "mixed-D64": (64, units_of([100, 37, 5], 64, 2, prior=[200, 0, 50])),
+    "noncausal-D128": (128, units_of([40, 3, 77], 128, 8, prior=[300, 10, 0], causal=False)),
 }
 
 
-@pytest.mark.parametrize("nprod", [4, 6, 8])
-@pytest.mark.parametrize("case", sorted(CASES))
-def test_protocol_has_no_stale_wait_or_overwrite(case, nprod):
+def _run(case, kp, vp, seeds, mutate=None):
     D, units = CASES[case]
-    for seed in range(25):
+    for seed in seeds:
         order = list(units)
         random.Random(seed).shuffle(order)
-        simulate(D, order[:48], nprod, seed)
+        simulate(D, order[:48], kp, vp, seed, mutate=mutate)
 
 
-def test_the_model_finds_the_earlier_claim_order_defect():
-    """Issuing the previous unit's last PV first only when the new Q has not
-    landed frees ring positions out of order; with producers far enough ahead
-    a parity wait then passes on a phase still open."""
-    D, units = CASES["prefill-D256"]
-    found = False
-    for seed in range(40):
-        order = list(units)
-        random.Random(seed).shuffle(order)
-        try:
-            simulate(D, order[:48], 6, seed, order="dynamic")
-        except (StaleWait, AssertionError):
-            found = True
-            break
-    assert found
+@pytest.mark.parametrize("kp,vp", [(2, 2), (1, 1), (3, 3)])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_protocol_has_no_stale_wait_or_overwrite(case, kp, vp):
+    _run(case, kp, vp, range(20))
+
+
+@pytest.mark.parametrize("mutate,case,seeds", [
+    ("no_sbuf_wait", "prefill-D256", range(20)),
+    ("no_vtail_wait", "ragged-D256", range(200)),
+])
+def test_the_model_finds_planted_mistakes(mutate, case, seeds):
+    with pytest.raises(AssertionError):
+        _run(case, 2, 2, seeds, mutate=mutate)
