@@ -683,33 +683,34 @@ __global__ void __launch_bounds__(480, 1)
             __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(a.out) +
                                   (((int64_t)u.c0 + qi) * Hq + (int64_t)u.h * G + g) * D +
                                   wg * (D / 2);
-#pragma unroll 1
-            for (int c = 0; c < D / 64; ++c) {
-                float o[32];
-                if (u.ntiles > 0) {
-                    tmem_ld32(o_lane + 32 * c, o);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0.f;
-                }
-                if (row_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(
-                            pack_bf16x2(o[8 * q + 0] * scale_out, o[8 * q + 1] * scale_out),
-                            pack_bf16x2(o[8 * q + 2] * scale_out, o[8 * q + 3] * scale_out),
-                            pack_bf16x2(o[8 * q + 4] * scale_out, o[8 * q + 5] * scale_out),
-                            pack_bf16x2(o[8 * q + 6] * scale_out, o[8 * q + 7] * scale_out));
-                }
-            }
+            // O is read out of TMEM into packed bf16 registers first, two 32-column
+            // loads in flight, and handed back to the PV issuer before the stores
+            uint32_t pk[D / 4];   // this thread's D / 2 outputs, two per register
             if (u.ntiles > 0) {
+#pragma unroll
+                for (int c = 0; c < D / 64; c += 2) {
+                    float o[64];
+                    tmem_ld32(o_lane + 32 * c, o);
+                    if (c + 1 < D / 64) tmem_ld32(o_lane + 32 * (c + 1), o + 32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32 * min(2, D / 64 - c); e += 2)
+                        pk[16 * c + e / 2] = pack_bf16x2(o[e] * scale_out, o[e + 1] * scale_out);
+                }
                 // O may now be overwritten by the unit NOB ahead
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_o_free + 8 * ob);
                 ++itn;
+            } else {
+#pragma unroll
+                for (int e = 0; e < D / 4; ++e) pk[e] = 0u;   // no key visible: zeros
+            }
+            if (row_ok) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow);
+#pragma unroll
+                for (int q = 0; q < D / 16; ++q)
+                    dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
         }
     }
