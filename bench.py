@@ -59,7 +59,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel sources whose hash is recorded beside it: the files that define that
 # kernel.  Reported as null once they change, until a new capture is taken.
 NCU_TRAFFIC = {"sources_sha256": "d3429d45005de5736aa6f83c597123fbdc0d7f80fa4a1384a92ff3edd2021eeb",
-               "bytes_per_launch": 526309632 + 5093888, "workload": 1,
+               "bytes_per_launch": 526285312 + 5297152, "workload": 1,
                "kernel": "paged_decode_tc_kernel"}
 TRAFFIC_SOURCES = ("decode_tc.cuh", "decode_tc_d128.cu", "pa_common.cuh", "tc_common.cuh")
 
@@ -276,12 +276,27 @@ def cpu_baseline(w, kind, budget_s=8.0, budget_1core_s=4.0):
             "single_core": {"value": round(v1, 6), "unit": unit, "cores": 1, "sample": sample1}}
 
 
-def workload_config(w, widx, P_used, layout, step, world, work):
+L2_BYTES = 126e6          # GB300 L2 (the device reports ~126 MB)
+FLUSH_BYTES = 256 << 20   # written between timed steps when a step's data fits in L2
+
+
+def needs_l2_flush(w, work) -> bool:
+    """A step whose K/V, queries and outputs fit in L2 twice over would find
+    them resident from the step before: such steps are timed with an L2 flush
+    between them."""
+    e = 2 if w.dtype == "bf16" else 4
+    return work["kv"] + 2 * w.total_q * w.num_q_heads * w.head_dim * e < 2 * L2_BYTES
+
+
+def workload_config(w, widx, P_used, layout, step, world, work, flushed=None):
+    if flushed is None:
+        flushed = needs_l2_flush(w, work)
     return {"workload": WORKLOAD_NAMES_CACHE[widx], "num_seqs": w.num_seqs,
             "total_q": w.total_q, "total_kv_tokens": int(w.seq_lens.sum()),
             "partition_size": P_used,
-            "l2": "no flush: the KV read per step exceeds the 126 MB L2"
-                  if work["kv"] > 2 * 126e6 else "no flush (KV partly L2-resident)",
+            "l2": (f"flushed between timed steps ({FLUSH_BYTES >> 20} MB write, outside the "
+                   "per-step events)") if flushed
+                  else "no flush: the data a step reads exceeds twice the 126 MB L2",
             "parallelism": f"independent batch per GPU x{world}",
             "layout": layout, "step": step}
 
@@ -400,6 +415,8 @@ def measure(args, widx, rank, world, local, with_cpu_baseline):
             dist.barrier()
 
     steps = args.steps
+    flush = needs_l2_flush(w, work)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device) if flush else None
     # ---------------- device-resident timing
     for _ in range(args.warmup):
         scatter()
@@ -415,6 +432,8 @@ def measure(args, widx, rank, world, local, with_cpu_baseline):
     clocks.mark_on()
     start.record(stream)
     for i in range(steps):
+        if flush:
+            flush_buf.fill_(i & 255)   # evicts the previous step's data from L2
         ev[i][0].record(stream)
         scatter()
         ev[i][1].record(stream)
@@ -427,7 +446,11 @@ def measure(args, widx, rank, world, local, with_cpu_baseline):
     torch.cuda.synchronize()
     clk = clocks.stop()
     assert pa.pa_device_error() == 0, "device error word set during the benchmark"
-    elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, device)
+    if flush:   # the steps alone: from each step's first event to its last
+        elapsed_s = max_over_ranks(sum(ev[i][0].elapsed_time(ev[i][2]) for i in range(steps))
+                                   / 1e3, world, device)
+    else:
+        elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, device)
     attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
     attn_avg_s = max_over_ranks(sum(attn_ms) / len(attn_ms) / 1e3, world, device)
     step_s = elapsed_s / steps
@@ -515,7 +538,8 @@ def measure(args, widx, rank, world, local, with_cpu_baseline):
         "data": "synthetic (seeded N(0,1) Q/K/V)",
         "config": workload_config(w_useful, widx, P_used, args.layout,
                                   "pa_scatter_and_attend" if fused
-                                  else "pa_reshape_and_cache + pa_varlen_attention", world, work),
+                                  else "pa_reshape_and_cache + pa_varlen_attention", world, work,
+                                  flushed=flush),
         "kv_gbs": round(world * work["step_bytes"] / step_s / 1e9, 2),
         "tflops": round(world * work["flops"] / step_s / 1e12, 3),
         "tokens_per_s": round(world * w_useful.total_q / step_s, 1),
@@ -527,7 +551,7 @@ def measure(args, widx, rank, world, local, with_cpu_baseline):
     }
     if rank == 0 and world == 1 and with_cpu_baseline:
         rec["cpu_baseline"] = cpu_baseline(w_useful, kind)
-    del q, kc, vc, nk, nv, out, ws, stage
+    del q, kc, vc, nk, nv, out, ws, stage, flush_buf
     torch.cuda.empty_cache()
     return rec
 
@@ -548,12 +572,18 @@ def run_ours(args, rank, world, local):
     line = measure(args, primary, rank, world, local, with_cpu)
     if args.workload is None and not args.only_primary:
         subs = {}
+        keep = ("value", "unit", "ms_per_step", "dtype", "config", "kv_gbs", "tflops",
+                "tokens_per_s", "roofline", "e2e", "gpu_launches", "clocks", "cpu_baseline")
         for widx in (2, 3, 4):
             rec = measure(args, widx, rank, world, local, with_cpu)
-            keep = ("value", "unit", "ms_per_step", "dtype", "config", "kv_gbs", "tflops",
-                    "tokens_per_s", "roofline", "e2e", "gpu_launches", "clocks",
-                    "cpu_baseline")
             subs[str(widx)] = {k: rec[k] for k in keep if k in rec}
+        # the prefill batch laid out padded ([B, T_max]: every request padded to
+        # the longest), useful work counted: what packing is worth on this mix
+        padded_args = argparse.Namespace(**vars(args))
+        padded_args.layout = "padded"
+        padded_args.steps = min(args.steps, 500)
+        rec = measure(padded_args, 2, rank, world, local, False)
+        subs["2_padded"] = {k: rec[k] for k in keep if k in rec}
         line["workloads"] = subs
     if rank == 0:
         print(json.dumps(line), flush=True)

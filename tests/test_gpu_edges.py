@@ -160,3 +160,17 @@ def test_scatter_and_attend_full_size_matches_oracle(widx):
         c0, c1 = int(w.cu_seqlens_q[r]), int(w.cu_seqlens_q[r + 1])
         rows.extend(range(c0, c1) if c1 - c0 <= 5 else [c0, c1 - 1] + rng.integers(c0, c1, 2).tolist())
     _fused_vs_oracle(w, rows=sorted(set(rows)))
+
+
+# ---------------------------------------------------------------- padded layout
+@pytest.mark.parametrize("D,Hq,Hkv", [(256, 16, 2), (128, 8, 2), (64, 4, 4)])
+def test_padded_layout_matches_oracle(D, Hq, Hkv):
+    """The same ragged batch laid out padded ([B, T_max]: every request gets
+    the longest request's query rows and keys, the layout a padded attention
+    computes on; aisignalhub.me, "packed queries and paged KV", batch A vs B)
+    runs through the same call and matches the oracle on every row."""
+    small = wl.random_small(180 + D, dtype=wl.BF16, num_seqs=5, num_q_heads=Hq,
+                            num_kv_heads=Hkv, head_dim=D, max_prior=0, max_q=90)
+    w = wl.padded(small)
+    assert len(set(w.q_lens.tolist())) == 1 and w.total_q == w.num_seqs * int(w.q_lens[0])
+    check_step(w)
