@@ -188,6 +188,54 @@ pa_status pa_scatter_and_attend(const void *key, const void *value, int64_t kv_t
                                 pa_dtype dtype, void *stream);
 
 /*
+ * The quantised KV cache (the layered-architecture page, lqnn.cn section 5,
+ * lists TurboQuant helpers for the KV cache without a format; this library's
+ * reading): each token's K row and V row of one KV head is stored as D 8-bit
+ * floats E4M3 (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinity, largest 448) plus one float32 scale:
+ *   amax  = max_d |x_d|,  inv = 448 / amax  (float32 division),
+ *   code  = E4M3(x_d * inv)  (float32 product, round to nearest even,
+ *                             saturating at 448),
+ *   scale = amax / 448  (float32 division); a row of zeros: codes 0, scale 0.
+ * The row stands for value(code_d) * scale.  Layouts: codes
+ * [num_blocks, block_size, H_kv, D] uint8 (the bf16 cache's layout, one byte
+ * per element), scales [num_blocks, block_size, H_kv] float32.  head_dim 128
+ * or 256.
+ *
+ * pa_reshape_and_cache_fp8 -- reshape_and_cache into the quantised cache: for
+ * each token t with slot s = slot_mapping[t] >= 0 (and < num_blocks *
+ * block_size; others are skipped), quantises key[t] and value[t] ([H_kv, D]
+ * rows, bf16 or float32 per `dtype`, token stride kv_token_stride elements)
+ * into the codes and scales of slot s.  Key and value rows start on 4-element
+ * boundaries; codes and scales are 4-byte aligned.  Returns PA_OK,
+ * PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED (head_dim), PA_ERR_CUDA.
+ */
+pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t kv_token_stride,
+                                   void *key_codes, void *value_codes, float *key_scales,
+                                   float *value_scales, const int64_t *slot_mapping,
+                                   int64_t num_tokens, int num_kv_heads, int head_dim,
+                                   int block_size, int64_t num_blocks, pa_dtype dtype,
+                                   void *stream);
+
+/*
+ * pa_varlen_attention_fp8kv -- pa_varlen_attention over the quantised cache:
+ * the same packed rows, masking, sinks, split-KV plan, workspace (sized by
+ * pa_varlen_attention_workspace_size) and result, with every key and value
+ * row taken as value(code) * scale.  q and out are bf16 (`dtype` must be
+ * PA_BF16).  The arithmetic is float32 on the CUDA cores (single-query rows
+ * split over partitions and merged by the shared reduce, multi-query rows one
+ * CTA per row and KV head).  Returns the statuses of pa_varlen_attention, and
+ * PA_ERR_UNSUPPORTED for another dtype or head_dim.
+ */
+pa_status pa_varlen_attention_fp8kv(
+    void *out, const void *q, const void *key_codes, const void *value_codes,
+    const float *key_scales, const float *value_scales, const int32_t *cu_seqlens_q,
+    const int32_t *seq_lens_k, const int32_t *block_tables, int max_blocks_per_seq, int num_seqs,
+    int64_t total_q, int max_seqlen_q, int max_seqlen_k, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int64_t num_blocks, float scale, const float *sinks, int causal,
+    int partition_size, void *workspace, size_t workspace_bytes, pa_dtype dtype, void *stream);
+
+/*
  * pa_split_kv_reduce -- the shared reduce of split-KV partials.
  * (kwkr.cn trick 4: partials are a log2-space (max, exp-sum) pair plus a
  * normalised partial output, merged by one shared reduce kernel.)

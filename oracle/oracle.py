@@ -51,6 +51,15 @@ def _load():
                                               I, L, D]
         lib.oracle_split_combine.restype = I
         lib.oracle_split_combine.argtypes = [P, P, P, P, I, I, I, P, P, I, I, I, P]
+        lib.oracle_paged_attention_kv.restype = I
+        lib.oracle_paged_attention_kv.argtypes = [P, P, L, P, P, P, I, I, P, P, P, I, I, I, I, I,
+                                                  I, L, D, P, I, I]
+        lib.oracle_e4m3_value.restype = D
+        lib.oracle_e4m3_value.argtypes = [I]
+        lib.oracle_e4m3_encode.restype = I
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_quantize_kv_fp8.restype = I
+        lib.oracle_quantize_kv_fp8.argtypes = [P, P, L, P, P, P, P, P, L, I, I, I, L, I]
         _lib = lib
     return _lib
 
@@ -164,4 +173,73 @@ def split_combine(part_o, part_m, part_l, cu_seqlens_q, seq_lens_k, *, partition
                                   _ptr(_c(seq_lens_k, np.int32)), S, Hq, D, _ptr(sk))
     if rc:
         raise ValueError(f"oracle_split_combine failed (rc={rc})")
+    return out
+
+
+# ---------------------------------------------------------------- quantised KV cache
+def e4m3_values() -> np.ndarray:
+    """The number each of the 256 E4M3 codes stands for (float64; NaN codes NaN)."""
+    lib = _load()
+    return np.array([lib.oracle_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """E4M3 codes of float32 values (nearest, ties to even, saturated at 448)."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib.oracle_e4m3_encode(float(x)) for x in v], dtype=np.uint8)
+
+
+def quantize_kv_fp8(new_k, new_v, key_codes, value_codes, key_scales, value_scales,
+                    slot_mapping, block_size: int, dtype: str):
+    """Scatter new_k/new_v [T, H_kv, D] (bf16 bits or float32) into copies of the
+    quantised pools (codes [num_blocks, bs, H_kv, D] uint8, scales
+    [num_blocks, bs, H_kv] float32); returns the four new arrays."""
+    lib = _load()
+    kc = np.array(key_codes, dtype=np.uint8, copy=True, order="C")
+    vc = np.array(value_codes, dtype=np.uint8, copy=True, order="C")
+    ks = np.array(key_scales, dtype=np.float32, copy=True, order="C")
+    vs = np.array(value_scales, dtype=np.float32, copy=True, order="C")
+    nk = np.ascontiguousarray(new_k)
+    nv = np.ascontiguousarray(new_v)
+    sm = _c(slot_mapping, np.int64)
+    T, Hkv, D = nk.shape
+    rc = lib.oracle_quantize_kv_fp8(_ptr(nk), _ptr(nv), Hkv * D, _ptr(kc), _ptr(vc), _ptr(ks),
+                                    _ptr(vs), _ptr(sm), T, Hkv, D, block_size, kc.shape[0],
+                                    _DTYPE_CODE[dtype])
+    if rc:
+        raise ValueError(f"oracle_quantize_kv_fp8: slot outside the pool (rc={rc})")
+    return kc, vc, ks, vs
+
+
+def dequantize_kv_fp8(codes, scales) -> np.ndarray:
+    """value(code) * scale for a quantised pool, exactly (float64)."""
+    table = e4m3_values()
+    return table[np.asarray(codes, dtype=np.uint8)] * np.asarray(scales, np.float64)[..., None]
+
+
+def paged_attention_kv(q, key_cache_f64, value_cache_f64, cu_seqlens_q, seq_lens_k,
+                       block_tables, *, q_dtype: str, num_q_heads: int, num_kv_heads: int,
+                       head_dim: int, block_size: int, scale: float, causal: bool, sinks=None,
+                       rows: Optional[Sequence[int]] = None, nthreads: Optional[int] = None):
+    """fp64 attention of q (bf16 bits or float32) over float64 pools (a
+    dequantised cache), for the query rows in ``rows`` (default: all)."""
+    lib = _load()
+    q = np.ascontiguousarray(q)
+    rows = np.arange(q.shape[0], dtype=np.int64) if rows is None else _c(rows, np.int64)
+    out = np.zeros((len(rows), num_q_heads, head_dim), dtype=np.float64)
+    cu = _c(cu_seqlens_q, np.int32)
+    sl = _c(seq_lens_k, np.int32)
+    bt = _c(block_tables, np.int32)
+    kc = _c(key_cache_f64, np.float64)
+    vc = _c(value_cache_f64, np.float64)
+    sk = None if sinks is None else _c(sinks, np.float64)
+    nthreads = nthreads or os.cpu_count() or 1
+    rc = lib.oracle_paged_attention_kv(_ptr(out), _ptr(rows), len(rows), _ptr(q), _ptr(kc),
+                                       _ptr(vc), _DTYPE_CODE[q_dtype], 2, _ptr(cu), _ptr(sl),
+                                       _ptr(bt), bt.shape[1], len(sl), num_q_heads, num_kv_heads,
+                                       head_dim, block_size, kc.shape[0], float(scale), _ptr(sk),
+                                       int(bool(causal)), int(nthreads))
+    if rc:
+        raise ValueError(f"oracle_paged_attention_kv failed (rc={rc})")
     return out

@@ -32,7 +32,8 @@
  *  - a row that sees no key outputs zeros;
  *  - a negative slot in slot_mapping is a padding token and is skipped.
  *
- * dtype codes: 0 = float32, 1 = bfloat16 (stored as uint16 bit patterns).
+ * dtype codes: 0 = float32, 1 = bfloat16 (stored as uint16 bit patterns),
+ * 2 = float64 (a dequantised 8-bit cache, see the quantised KV section).
  */
 #include <math.h>
 #include <pthread.h>
@@ -42,9 +43,11 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+#define ORACLE_F64 2
 
 static double elem(const void *base, int64_t idx, int dtype) {
     if (dtype == ORACLE_F32) return (double)((const float *)base)[idx];
+    if (dtype == ORACLE_F64) return ((const double *)base)[idx];
     /* a bf16 value is the top half of the float32 with the same bits */
     uint32_t u = (uint32_t)((const uint16_t *)base)[idx] << 16;
     float f;
@@ -84,7 +87,8 @@ typedef struct {
     const int64_t *rows;    /* [n_sel] global query rows */
     int64_t n_sel;
     const void *q, *key_cache, *value_cache;
-    int dtype;
+    int dtype;              /* of q */
+    int kv_dtype;           /* of the caches */
     const int32_t *cu_seqlens_q, *seq_lens_k, *block_tables;
     int max_blocks_per_seq, num_seqs;
     int num_q_heads, num_kv_heads, head_dim, block_size;
@@ -138,7 +142,7 @@ static int attend_one(const attn_job *a, int64_t sel, int h, double *s_buf) {
         if (ko < 0) return -1;
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
-            dot += elem(a->q, qoff + d, a->dtype) * elem(a->key_cache, ko + d, a->dtype);
+            dot += elem(a->q, qoff + d, a->dtype) * elem(a->key_cache, ko + d, a->kv_dtype);
         s_buf[j] = a->scale * dot;
         if (s_buf[j] > m) m = s_buf[j];
     }
@@ -151,7 +155,7 @@ static int attend_one(const attn_job *a, int64_t sel, int h, double *s_buf) {
         double p = exp(s_buf[j] - m);
         den += p;
         int64_t vo = kv_offset(a, r, j, g);
-        for (int d = 0; d < D; ++d) o[d] += p * elem(a->value_cache, vo + d, a->dtype);
+        for (int d = 0; d < D; ++d) o[d] += p * elem(a->value_cache, vo + d, a->kv_dtype);
     }
     if (a->sinks) den += exp(sink - m);
     for (int d = 0; d < D; ++d) o[d] /= den;
@@ -181,13 +185,13 @@ static void *attn_worker(void *arg) {
  * Returns 0; -1 bad page id; -2 row outside cu_seqlens_q; -3 seq_len larger
  * than the block table; -4 out of memory.
  */
-int oracle_paged_attention(double *out, const int64_t *rows, int64_t n_sel, const void *q,
-                           const void *key_cache, const void *value_cache, int dtype,
-                           const int32_t *cu_seqlens_q, const int32_t *seq_lens_k,
-                           const int32_t *block_tables, int max_blocks_per_seq, int num_seqs,
-                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                           int64_t num_blocks, double scale, const double *sinks, int causal,
-                           int nthreads) {
+int oracle_paged_attention_kv(double *out, const int64_t *rows, int64_t n_sel, const void *q,
+                              const void *key_cache, const void *value_cache, int dtype,
+                              int kv_dtype, const int32_t *cu_seqlens_q,
+                              const int32_t *seq_lens_k, const int32_t *block_tables,
+                              int max_blocks_per_seq, int num_seqs, int num_q_heads,
+                              int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                              double scale, const double *sinks, int causal, int nthreads) {
     if (nthreads < 1) nthreads = 1;
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads) return -2;
     attn_job *jobs = (attn_job *)calloc((size_t)nthreads, sizeof(attn_job));
@@ -197,6 +201,7 @@ int oracle_paged_attention(double *out, const int64_t *rows, int64_t n_sel, cons
         attn_job *a = &jobs[t];
         a->out = out; a->rows = rows; a->n_sel = n_sel; a->q = q;
         a->key_cache = key_cache; a->value_cache = value_cache; a->dtype = dtype;
+        a->kv_dtype = kv_dtype;
         a->cu_seqlens_q = cu_seqlens_q; a->seq_lens_k = seq_lens_k;
         a->block_tables = block_tables; a->max_blocks_per_seq = max_blocks_per_seq;
         a->num_seqs = num_seqs; a->num_q_heads = num_q_heads; a->num_kv_heads = num_kv_heads;
@@ -217,6 +222,20 @@ int oracle_paged_attention(double *out, const int64_t *rows, int64_t n_sel, cons
         if (jobs[t].error && !rc) rc = jobs[t].error;
     free(started); free(jobs); free(th);
     return rc;
+}
+
+/* The same, with the caches in the dtype of q. */
+int oracle_paged_attention(double *out, const int64_t *rows, int64_t n_sel, const void *q,
+                           const void *key_cache, const void *value_cache, int dtype,
+                           const int32_t *cu_seqlens_q, const int32_t *seq_lens_k,
+                           const int32_t *block_tables, int max_blocks_per_seq, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int64_t num_blocks, double scale, const double *sinks, int causal,
+                           int nthreads) {
+    return oracle_paged_attention_kv(out, rows, n_sel, q, key_cache, value_cache, dtype, dtype,
+                                     cu_seqlens_q, seq_lens_k, block_tables, max_blocks_per_seq,
+                                     num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                     num_blocks, scale, sinks, causal, nthreads);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -331,5 +350,97 @@ int oracle_split_combine(double *out, const void *part_o, const void *part_m,
         }
     }
 #undef PART
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Quantised KV cache.  The layered-architecture page (lqnn.cn, section 5)   */
+/* lists TurboQuant helpers for the KV cache without a format; the reading   */
+/* taken here: each token's K (and V) row of one KV head is stored as 8-bit  */
+/* floats E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no    */
+/* infinity, max 448) with one float32 scale per (token, KV head):          */
+/*   amax  = max_d |x_d|                    (x as float32)                   */
+/*   inv   = 448 / amax                     (float32 division)              */
+/*   code  = E4M3(x_d * inv)                (float32 product, rounded to     */
+/*                                           nearest even, saturated at 448) */
+/*   scale = amax / 448                     (float32 division)              */
+/* and a row of zeros stores codes 0 with scale 0.  The value a code stands  */
+/* for is value(code) * scale, taken exactly (float64 here).                 */
+/* ------------------------------------------------------------------------- */
+
+/* The number an E4M3 code stands for (NaN for the codes S.1111.111). */
+double oracle_e4m3_value(int code) {
+    const int sign = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);                 /* subnormal */
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to v (a float32), ties to the even code, |v| above the  */
+/* largest finite value saturating to it, the sign kept (a negative value    */
+/* too small for the smallest subnormal gives negative zero).  The finite    */
+/* non-negative codes 0 .. 0x7E stand for increasing values, so the nearest  */
+/* is one of the two codes around |v| (found by bisection).                  */
+int oracle_e4m3_encode(float v) {
+    const double x = fabs((double)v);
+    int best;
+    if (x >= 448.0) {
+        best = 0x7E;
+    } else {
+        int lo = 0, hi = 0x7E;                /* value(lo) <= x < value(hi) */
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) / 2;
+            if (oracle_e4m3_value(mid) <= x) lo = mid;
+            else hi = mid;
+        }
+        const double elo = x - oracle_e4m3_value(lo), ehi = oracle_e4m3_value(hi) - x;
+        best = (elo < ehi || (elo == ehi && (lo & 1) == 0)) ? lo : hi;
+    }
+    return signbit(v) ? (best | 0x80) : best;
+}
+
+/* reshape_and_cache into the quantised cache: for each token t with slot   */
+/* s = slot_mapping[t] >= 0, for each KV head h, the row of key (value) is   */
+/* quantised into key_codes[(s * H_kv + h) * D + d] and key_scales[s * H_kv   */
+/* + h].  Returns 0, or -1 if a slot lies outside the pool.                  */
+int oracle_quantize_kv_fp8(const void *key, const void *value, int64_t kv_token_stride,
+                           uint8_t *key_codes, uint8_t *value_codes, float *key_scales,
+                           float *value_scales, const int64_t *slot_mapping, int64_t num_tokens,
+                           int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                           int in_dtype) {
+    const int D = head_dim;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue; /* padding token */
+        if (slot >= num_blocks * block_size) return -1;
+        for (int which = 0; which < 2; ++which) {
+            const void *src = which ? value : key;
+            uint8_t *codes = which ? value_codes : key_codes;
+            float *scales = which ? value_scales : key_scales;
+            for (int h = 0; h < num_kv_heads; ++h) {
+                const int64_t in0 = t * kv_token_stride + (int64_t)h * D;
+                const int64_t out0 = (slot * num_kv_heads + h) * D;
+                float amax = 0.0f;
+                for (int d = 0; d < D; ++d) {
+                    const float x = (float)elem(src, in0 + d, in_dtype);
+                    if (fabsf(x) > amax) amax = fabsf(x);
+                }
+                if (amax == 0.0f) {
+                    for (int d = 0; d < D; ++d) codes[out0 + d] = 0;
+                    scales[slot * num_kv_heads + h] = 0.0f;
+                    continue;
+                }
+                const float inv = 448.0f / amax;
+                for (int d = 0; d < D; ++d) {
+                    const float x = (float)elem(src, in0 + d, in_dtype);
+                    const float y = x * inv;
+                    codes[out0 + d] = (uint8_t)oracle_e4m3_encode(y);
+                }
+                scales[slot * num_kv_heads + h] = amax / 448.0f;
+            }
+        }
+    }
     return 0;
 }

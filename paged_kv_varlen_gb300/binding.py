@@ -63,6 +63,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pa_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.pa_test_expire_next_wait.restype = None
     lib.pa_test_expire_next_wait.argtypes = []
+    lib.pa_reshape_and_cache_fp8.restype = I
+    lib.pa_reshape_and_cache_fp8.argtypes = [P, P, L, P, P, P, P, P, L, I, I, I, L, I, P]
+    lib.pa_varlen_attention_fp8kv.restype = I
+    lib.pa_varlen_attention_fp8kv.argtypes = [P, P, P, P, P, P, P, P, P, I, I, L, I, I, I, I, I,
+                                              I, L, F, P, I, I, P, S, I, P]
     _lib = lib
     return lib
 
@@ -253,4 +258,63 @@ def pa_varlen_attention_static_scratch(out: torch.Tensor, q: torch.Tensor,
             total_q, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, bs, nb, float(scale),
             _ptr(sinks), int(bool(causal)), int(partition_size), _dtype(q), _stream(stream))
     _check(st, "pa_varlen_attention_static_scratch")
+    return out
+
+
+# ---------------------------------------------------------------- quantised KV cache
+def pa_reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, key_codes: torch.Tensor,
+                             value_codes: torch.Tensor, key_scales: torch.Tensor,
+                             value_scales: torch.Tensor, slot_mapping: torch.Tensor, *,
+                             stream=None):
+    """key/value [T, H_kv, D] (bf16 or float32; rows may be strided), codes
+    [num_blocks, block_size, H_kv, D] uint8, scales [num_blocks, block_size,
+    H_kv] float32, slot_mapping [T] int64."""
+    lib = load_library()
+    T, Hkv, D = key.shape
+    nb, bs = key_codes.shape[0], key_codes.shape[1]
+    if key.stride() != value.stride() or key.stride(2) != 1 or key.stride(1) != D:
+        raise PAError("key/value rows must be [H_kv, D]-contiguous with equal strides")
+    if slot_mapping.dtype != torch.int64:
+        raise PAError("slot_mapping must be int64")
+    if key_codes.dtype != torch.uint8 or key_scales.dtype != torch.float32:
+        raise PAError("codes must be uint8 and scales float32")
+    st = lib.pa_reshape_and_cache_fp8(ctypes.c_void_p(key.data_ptr()),
+                                      ctypes.c_void_p(value.data_ptr()), key.stride(0),
+                                      _ptr(key_codes), _ptr(value_codes), _ptr(key_scales),
+                                      _ptr(value_scales), _ptr(slot_mapping), T, Hkv, D, bs, nb,
+                                      _dtype(key), _stream(stream))
+    _check(st, "pa_reshape_and_cache_fp8")
+
+
+def pa_varlen_attention_fp8kv(out: torch.Tensor, q: torch.Tensor, key_codes: torch.Tensor,
+                              value_codes: torch.Tensor, key_scales: torch.Tensor,
+                              value_scales: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                              seq_lens_k: torch.Tensor, block_tables: torch.Tensor, *,
+                              max_seqlen_q: int, max_seqlen_k: int, scale: float,
+                              sinks: Optional[torch.Tensor] = None, causal: bool = True,
+                              partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                              stream=None) -> torch.Tensor:
+    """pa_varlen_attention over the quantised cache (codes uint8 [num_blocks,
+    block_size, H_kv, D], scales float32 [num_blocks, block_size, H_kv]); q/out
+    bf16."""
+    lib = load_library()
+    total_q, Hq, D = q.shape
+    nb, bs, Hkv, _ = key_codes.shape
+    S = seq_lens_k.shape[0]
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("seq_lens_k", seq_lens_k),
+                    ("block_tables", block_tables)):
+        if t.dtype != torch.int32:
+            raise PAError(f"{name} must be int32")
+    if sinks is not None and sinks.dtype != torch.float32:
+        raise PAError("sinks must be float32")
+    if workspace is None:
+        nbytes = pa_varlen_attention_workspace_size(S, max_seqlen_k, Hq, D, partition_size)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    st = lib.pa_varlen_attention_fp8kv(
+        _ptr(out), _ptr(q), _ptr(key_codes), _ptr(value_codes), _ptr(key_scales),
+        _ptr(value_scales), _ptr(cu_seqlens_q), _ptr(seq_lens_k), _ptr(block_tables),
+        block_tables.shape[1], S, total_q, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, bs,
+        nb, float(scale), _ptr(sinks), int(bool(causal)), int(partition_size), _ptr(workspace),
+        workspace.numel(), _dtype(q), _stream(stream))
+    _check(st, "pa_varlen_attention_fp8kv")
     return out

@@ -39,9 +39,14 @@ struct DecodeCfg {
     static constexpr int TK = decode_tile_keys(E, D);         // keys per tile
     static constexpr int LPK = 32 / TK;                       // lanes per key (QK)
     static constexpr int CPK = CPR / LPK;                     // chunks per lane (QK)
-    static constexpr int LPR = CPR < 32 ? CPR : 32;           // lanes per row (PV)
+    // PV reads value rows in pieces of PVB bytes: 16, or 8 for 8-bit codes so
+    // that a lane's accumulators cover 8 elements as with bf16
+    static constexpr int PVB = E == 1 ? 8 : 16;
+    static constexpr int VPV = PVB / E;                       // elements per PV piece
+    static constexpr int PPR = D * E / PVB;                   // PV pieces per row
+    static constexpr int LPR = PPR < 32 ? PPR : 32;           // lanes per row (PV)
     static constexpr int KPS = 32 / LPR;                      // rows per PV step
-    static constexpr int CPL = CPR / LPR;                     // chunks per lane (PV)
+    static constexpr int CPL = PPR / LPR;                     // pieces per lane (PV)
     static constexpr int NW = 4;                              // consumer warps
     static constexpr int THREADS = (NW + 1) * 32;
     // CTAs per SM the register budget is sized for: large head groups keep more
@@ -66,16 +71,19 @@ struct DecodeCfg {
     // merge scratch (reuses the stage ring once it has drained)
     static constexpr int MERGE_BYTES = NW * G * (D + 2) * 4;
     static_assert(MERGE_BYTES <= NS * STAGE_BYTES, "merge scratch must fit in the ring");
-    static_assert(D % EPB == 0 && CPR % LPK == 0 && CPR % LPR == 0, "shape");
+    static_assert(D % EPB == 0 && CPR % LPK == 0 && PPR % LPR == 0, "shape");
     static_assert(LPK <= 4 && TK >= 8, "lane mapping needs 8..32 keys per tile");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, DecodeCfg<T, D, G>::MIN_CTAS)
+// T: queries and output (fp32 / bf16); KV: the caches (T, or fp8_e4m3 codes
+// with a float32 scale per (slot, KV head) row).
+template <typename T, int D, int G, typename KV = T>
+__global__ void __launch_bounds__(DecodeCfg<KV, D, G>::THREADS, DecodeCfg<KV, D, G>::MIN_CTAS)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-    using C = DecodeCfg<T, D, G>;
+    using C = DecodeCfg<KV, D, G>;
+    constexpr bool kScaled = Elem<KV>::kScaled;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -215,7 +223,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, DecodeCfg<T, D, G
 
     // ================================================================ consumers
     // Packed fp32x2 arithmetic: pairs of adjacent elements share one FFMA2.
-    constexpr int HV = C::VEC / 2;                     // element pairs per 16-B chunk
+    constexpr int HV = C::VPV / 2;                     // element pairs per PV piece
     float m[G], l[G];
     float2 acc[G][C::CPL * HV];
 #pragma unroll
@@ -242,6 +250,18 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, DecodeCfg<T, D, G
         const int cnt = min(C::TK, k1 - (k0 + t * C::TK));
         const uint32_t sk = ring + s * C::STAGE_BYTES;
         const uint32_t sv = sk + C::TILE_BYTES;
+        // quantised cache: the scales of this lane's key row (K) and value row (V)
+        float kscale = 1.f, vscale = 1.f;
+        if constexpr (kScaled) {
+            if (qk_key < cnt) {
+                const int key = k0 + t * C::TK + qk_key;
+                const int page =
+                    __ldg(a.block_tables + (int64_t)r * a.max_blocks_per_seq + key / bs);
+                const int64_t sidx = ((int64_t)page * bs + key % bs) * a.num_kv_heads + h;
+                kscale = __ldg(a.k_scales + sidx);
+                vscale = __ldg(a.v_scales + sidx);
+            }
+        }
 
         // ---- scores t_j = <q * scale * log2e, k_j> for this lane's key
         float2 sc2[G];
@@ -252,7 +272,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, DecodeCfg<T, D, G
             const int c = qk_half * C::CPK + i;
             const uint32_t addr = sk + (c >> 3) * (C::TK * 128) + qk_row + (((c & 7) ^ qk_x) << 4);
             float kf[C::VEC];
-            Elem<T>::unpack(lds128(addr), kf);
+            Elem<KV>::unpack(lds128(addr), kf);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float4 *qv = reinterpret_cast<const float4 *>(qs + g * D + c * C::VEC);
@@ -272,6 +292,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, DecodeCfg<T, D, G
             sc[g] = sc2[g].x + sc2[g].y;
             if (C::LPK > 1) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], 8);
             if (C::LPK > 2) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], 16);
+            if constexpr (kScaled) sc[g] *= kscale;   // <q, code_j> * scale_j
         }
         const bool valid = qk_key < cnt;
         // ---- one online-softmax update per tile (log2 domain)
@@ -285,7 +306,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, DecodeCfg<T, D, G
             const float pg = none ? 0.f : exp2f(sg - mnew);
             l[g] = l[g] * corr[g] + (qk_half == 0 ? pg : 0.f);
             m[g] = mnew;
-            if (qk_half == 0) psw[qk_key * C::GP + g] = make_float2(pg, pg);
+            // the PV weight carries the value row's scale (l counts p alone)
+            const float pw = kScaled ? pg * vscale : pg;
+            if (qk_half == 0) psw[qk_key * C::GP + g] = make_float2(pw, pw);
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -308,10 +331,14 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, DecodeCfg<T, D, G
             const int jx = j & 7;
 #pragma unroll
             for (int ci = 0; ci < C::CPL; ++ci) {
-                const int c = pv_lane + ci * C::LPR;
+                const int pc = pv_lane + ci * C::LPR;   // PV piece of the row
+                const int c = pc * C::PVB / 16;         // its 16-byte chunk
                 const uint32_t addr = row + (c >> 3) * (C::TK * 128) + (((c & 7) ^ jx) << 4);
-                float vf[C::VEC];
-                Elem<T>::unpack(lds128(addr), vf);
+                float vf[C::VPV];
+                if constexpr (C::PVB == 16)
+                    Elem<KV>::unpack(lds128(addr), vf);
+                else
+                    Elem<KV>::unpack8(lds64(addr + (pc & 1) * 8), vf);
 #pragma unroll
                 for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -362,7 +389,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, DecodeCfg<T, D, G
             for (int ci = 0; ci < C::CPL; ++ci)
 #pragma unroll
                 for (int e = 0; e < HV; ++e) {
-                    float *o = os + (warp * G + g) * D + (pv_lane + ci * C::LPR) * C::VEC + 2 * e;
+                    float *o = os + (warp * G + g) * D + (pv_lane + ci * C::LPR) * C::VPV + 2 * e;
                     o[0] = acc[g][ci * HV + e].x;
                     o[1] = acc[g][ci * HV + e].y;
                 }
@@ -408,11 +435,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, DecodeCfg<T, D, G
     }
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, typename KV = T>
 cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &a,
                             dim3 grid, cudaStream_t stream) {
-    using C = DecodeCfg<T, D, G>;
-    auto kern = paged_decode_kernel<T, D, G>;
+    using C = DecodeCfg<KV, D, G>;
+    auto kern = paged_decode_kernel<T, D, G, KV>;
     static bool configured = false;   // benign race: idempotent attribute set
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -424,18 +451,18 @@ cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &vmap, co
     return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int D, typename KV = T>
 cudaError_t launch_decode_group(int group, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                 const DecodeArgs &a, dim3 grid, cudaStream_t stream) {
     switch (group) {
-        case 1: return launch_decode_t<T, D, 1>(kmap, vmap, a, grid, stream);
-        case 2: return launch_decode_t<T, D, 2>(kmap, vmap, a, grid, stream);
-        case 3: return launch_decode_t<T, D, 3>(kmap, vmap, a, grid, stream);
-        case 4: return launch_decode_t<T, D, 4>(kmap, vmap, a, grid, stream);
-        case 5: return launch_decode_t<T, D, 5>(kmap, vmap, a, grid, stream);
-        case 6: return launch_decode_t<T, D, 6>(kmap, vmap, a, grid, stream);
-        case 7: return launch_decode_t<T, D, 7>(kmap, vmap, a, grid, stream);
-        case 8: return launch_decode_t<T, D, 8>(kmap, vmap, a, grid, stream);
+        case 1: return launch_decode_t<T, D, 1, KV>(kmap, vmap, a, grid, stream);
+        case 2: return launch_decode_t<T, D, 2, KV>(kmap, vmap, a, grid, stream);
+        case 3: return launch_decode_t<T, D, 3, KV>(kmap, vmap, a, grid, stream);
+        case 4: return launch_decode_t<T, D, 4, KV>(kmap, vmap, a, grid, stream);
+        case 5: return launch_decode_t<T, D, 5, KV>(kmap, vmap, a, grid, stream);
+        case 6: return launch_decode_t<T, D, 6, KV>(kmap, vmap, a, grid, stream);
+        case 7: return launch_decode_t<T, D, 7, KV>(kmap, vmap, a, grid, stream);
+        case 8: return launch_decode_t<T, D, 8, KV>(kmap, vmap, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -675,3 +675,209 @@ PA_API pa_status pa_device_error(int *code) {
     if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
     return PA_OK;
 }
+
+// ---------------------------------------------------------------- quantised KV cache
+namespace pa {
+
+// A 3-D map over an 8-bit code cache: as make_cache_map, one byte per element,
+// boxes 128 codes wide.
+static pa_status make_code_map(CUtensorMap *map, const void *codes, int head_dim,
+                               int num_kv_heads, int64_t pool_rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled unavailable");
+        return PA_ERR_CUDA;
+    }
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)pool_rows};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim, (cuuint64_t)head_dim * num_kv_heads};
+    cuuint32_t box[3] = {128, 1, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(codes), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled (codes) failed (%d)",
+                 (int)r);
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+}  // namespace pa
+
+PA_API pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
+                                          int64_t kv_token_stride, void *key_codes,
+                                          void *value_codes, float *key_scales,
+                                          float *value_scales, const int64_t *slot_mapping,
+                                          int64_t num_tokens, int num_kv_heads, int head_dim,
+                                          int block_size, int64_t num_blocks, pa_dtype dtype,
+                                          void *stream) {
+    auto fail = [](const char *why) {
+        set_last_error(why);
+        return PA_ERR_INVALID_ARG;
+    };
+    if (dtype != PA_F32 && dtype != PA_BF16) return fail("unknown dtype");
+    if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0)
+        return fail("negative or empty size");
+    if (head_dim != 128 && head_dim != 256) {
+        set_last_error("the quantised cache takes head_dim 128 or 256");
+        return PA_ERR_UNSUPPORTED;
+    }
+    if (kv_token_stride < (int64_t)num_kv_heads * head_dim)
+        return fail("kv_token_stride shorter than a token's row");
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_codes || !value_codes || !key_scales || !value_scales ||
+        !slot_mapping)
+        return fail("null pointer");
+    const int e = dtype == PA_F32 ? 4 : 2;
+    if (((reinterpret_cast<uintptr_t>(key) | reinterpret_cast<uintptr_t>(value)) % (e * 4)) ||
+        ((kv_token_stride * e) % (e * 4)) ||
+        ((reinterpret_cast<uintptr_t>(key_codes) | reinterpret_cast<uintptr_t>(value_codes) |
+          reinterpret_cast<uintptr_t>(key_scales) | reinterpret_cast<uintptr_t>(value_scales)) &
+         3))
+        return fail("rows must start on 4-element boundaries, codes and scales 4-byte aligned");
+    if (num_tokens * num_kv_heads > (int64_t)0x7fffffff * 8) {
+        set_last_error("too many (token, KV head) rows");
+        return PA_ERR_UNSUPPORTED;
+    }
+    cudaError_t err = launch_quantize_kv_fp8(
+        key, value, kv_token_stride, e, static_cast<uint8_t *>(key_codes),
+        static_cast<uint8_t *>(value_codes), key_scales, value_scales, slot_mapping, num_tokens,
+        num_kv_heads, head_dim, num_blocks * block_size, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "quantize_kv_fp8 launch");
+    return PA_OK;
+}
+
+PA_API pa_status pa_varlen_attention_fp8kv(
+    void *out, const void *q, const void *key_codes, const void *value_codes,
+    const float *key_scales, const float *value_scales, const int32_t *cu_seqlens_q,
+    const int32_t *seq_lens_k, const int32_t *block_tables, int max_blocks_per_seq, int num_seqs,
+    int64_t total_q, int max_seqlen_q, int max_seqlen_k, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int64_t num_blocks, float scale, const float *sinks, int causal,
+    int partition_size, void *workspace, size_t workspace_bytes, pa_dtype dtype, void *stream) {
+    // the attention call's checks (q and out in `dtype`, the code caches 16-byte aligned)
+    pa_status st = check_attention_args(out, q, key_codes, value_codes, cu_seqlens_q, seq_lens_k,
+                                        block_tables, max_blocks_per_seq, num_seqs, total_q,
+                                        max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads,
+                                        head_dim, block_size, num_blocks, sinks, partition_size,
+                                        dtype);
+    if (st != PA_OK) return st;
+    if (dtype != PA_BF16) {
+        set_last_error("the quantised cache takes bf16 queries and output");
+        return PA_ERR_UNSUPPORTED;
+    }
+    if (head_dim != 128 && head_dim != 256) {
+        set_last_error("the quantised cache takes head_dim 128 or 256");
+        return PA_ERR_UNSUPPORTED;
+    }
+    if (!key_scales || !value_scales ||
+        ((reinterpret_cast<uintptr_t>(key_scales) | reinterpret_cast<uintptr_t>(value_scales)) &
+         3)) {
+        set_last_error("key_scales / value_scales missing or not 4-byte aligned");
+        return PA_ERR_INVALID_ARG;
+    }
+    if (total_q == 0) return PA_OK;
+    const int group = num_q_heads / num_kv_heads;
+    DeviceInfo dev;
+    st = device_info(&dev);
+    if (st != PA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // split plan and workspace: the same layout as pa_varlen_attention's
+    const int P = pa_choose_partition_size(num_seqs, num_kv_heads, max_seqlen_k, partition_size,
+                                           dev.sm_count);
+    const int max_parts = (P > 0 && max_seqlen_k > 0) ? ceil_div(max_seqlen_k, P) : 1;
+    if (P > 0 && max_parts > kMaxReduceParts) {
+        snprintf(g_last_error, sizeof g_last_error,
+                 "%d split-KV partitions per request, at most %d", max_parts, kMaxReduceParts);
+        return PA_ERR_UNSUPPORTED;
+    }
+    float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
+    if (P > 0) {
+        const size_t plan_sz = align256(plan_bytes(num_seqs));
+        const SplitLayout L = split_layout(num_seqs, max_parts, num_q_heads, head_dim);
+        const size_t need = plan_sz + L.total;
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) {
+            snprintf(g_last_error, sizeof g_last_error,
+                     "this call needs %zu bytes of 16-byte aligned workspace (split-KV "
+                     "partition %d, %d partitions per request); %zu given%s",
+                     need, P, max_parts, workspace ? workspace_bytes : (size_t)0,
+                     workspace && !aligned16(workspace) ? " (misaligned)" : "");
+            return PA_ERR_WORKSPACE;
+        }
+        char *w = static_cast<char *>(workspace) + plan_sz;
+        part_o = reinterpret_cast<float *>(w);
+        part_m = reinterpret_cast<float *>(w + L.o_bytes);
+        part_l = reinterpret_cast<float *>(w + L.o_bytes + L.ml_bytes);
+    }
+
+    const int box_rows = gcd_int(decode_tile_keys(1, head_dim), block_size);
+    CUtensorMap kmap, vmap;
+    st = make_code_map(&kmap, key_codes, head_dim, num_kv_heads, num_blocks * block_size,
+                       box_rows);
+    if (st != PA_OK) return st;
+    st = make_code_map(&vmap, value_codes, head_dim, num_kv_heads, num_blocks * block_size,
+                       box_rows);
+    if (st != PA_OK) return st;
+
+    DecodeArgs a;
+    memset(&a, 0, sizeof a);
+    a.out = out;
+    a.q = q;
+    a.cu_seqlens_q = cu_seqlens_q;
+    a.seq_lens_k = seq_lens_k;
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.qscale = scale * kLog2e;
+    a.sinks = sinks;
+    a.causal = causal ? 1 : 0;
+    a.partition_size = P;
+    a.max_parts = max_parts;
+    a.part_o = part_o;
+    a.part_m = part_m;
+    a.part_l = part_l;
+    a.total_q = total_q;
+    a.err = dev.err;
+    a.box_rows = box_rows;
+    a.k_scales = key_scales;
+    a.v_scales = value_scales;
+    auto launch = [&](dim3 grid) -> cudaError_t {
+        return head_dim == 128 ? launch_decode_fp8kv_d128(group, kmap, vmap, a, grid, s)
+                               : launch_decode_fp8kv_d256(group, kmap, vmap, a, grid, s);
+    };
+    // single-query rows: one CTA per (partition, KV head, request)
+    a.mode = 0;
+    cudaError_t ce = launch(dim3(max_parts, num_kv_heads, num_seqs));
+    if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode (quantised) launch");
+    // rows of multi-query requests: one CTA per (row, KV head)
+    if (max_seqlen_q > 1) {
+        a.mode = 1;
+        ce = launch(dim3((unsigned)total_q, num_kv_heads, 1));
+        if (ce != cudaSuccess) return cuda_fail(ce, "paged_rows (quantised) launch");
+    }
+    if (P > 0) {
+        ReduceArgs ra;
+        memset(&ra, 0, sizeof ra);
+        ra.out = out;
+        ra.part_o = part_o;
+        ra.part_m = part_m;
+        ra.part_l = part_l;
+        ra.cu_seqlens_q = cu_seqlens_q;
+        ra.seq_lens_k = seq_lens_k;
+        ra.num_seqs = num_seqs;
+        ra.max_parts = max_parts;
+        ra.partition_size = P;
+        ra.num_q_heads = num_q_heads;
+        ra.sinks = sinks;
+        ra.meta_before_wait = 1;   // the kernels before it write only out / partials
+        ra.ncut = 0;
+        ra.group = group;
+        ce = launch_reduce(2, head_dim, ra, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "split_reduce launch");
+    }
+    return PA_OK;
+}

@@ -7,6 +7,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -156,6 +157,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -166,6 +173,7 @@ template <typename T> struct Elem;
 
 template <> struct Elem<float> {
     static constexpr int kVec = 4;
+    static constexpr bool kScaled = false;
     static __device__ __forceinline__ void unpack(const uint4 &u, float *f) {
         f[0] = __uint_as_float(u.x);
         f[1] = __uint_as_float(u.y);
@@ -178,6 +186,7 @@ template <> struct Elem<float> {
 
 template <> struct Elem<__nv_bfloat16> {
     static constexpr int kVec = 8;
+    static constexpr bool kScaled = false;
     // A bf16 value is the upper half of the float32 with the same bits.
     static __device__ __forceinline__ void unpack(const uint4 &u, float *f) {
         f[0] = __uint_as_float(u.x << 16);
@@ -194,6 +203,47 @@ template <> struct Elem<__nv_bfloat16> {
     }
     static __device__ __forceinline__ __nv_bfloat16 to_store(float x) {
         return __float2bfloat16_rn(x);
+    }
+};
+
+// An 8-bit float of the quantised KV cache (E4M3: 1 sign, 4 exponent and 3
+// mantissa bits, max 448); its rows carry a float32 scale per (token, KV head).
+struct fp8_e4m3 {
+    uint8_t bits;
+};
+
+template <> struct Elem<fp8_e4m3> {
+    static constexpr int kVec = 16;
+    static constexpr bool kScaled = true;
+    // 16 codes -> 16 floats (an E4M3 value is exact in half precision)
+    static __device__ __forceinline__ void unpack(const uint4 &u, float *f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+                    static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * j)) & 0xffffu), __NV_E4M3);
+                const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+                f[4 * i + 2 * j] = v.x;
+                f[4 * i + 2 * j + 1] = v.y;
+            }
+        }
+    }
+    // 8 codes -> 8 floats
+    static __device__ __forceinline__ void unpack8(const uint2 &u, float *f) {
+        const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+                    static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * j)) & 0xffffu), __NV_E4M3);
+                const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+                f[4 * i + 2 * j] = v.x;
+                f[4 * i + 2 * j + 1] = v.y;
+            }
+        }
     }
 };
 

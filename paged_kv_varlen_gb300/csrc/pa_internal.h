@@ -40,6 +40,10 @@ struct DecodeArgs {
     int64_t total_q;
     int *err;                  // device error word
     int box_rows;              // rows per TMA box: divides both kernels' tile lengths
+    // quantised cache only: float32 scale of each (slot, KV head)'s K and V row,
+    // [num_blocks * block_size, H_kv]; nullptr for bf16 / fp32 caches
+    const float *k_scales;
+    const float *v_scales;
 };
 
 // Arguments of the tensor-core kernel for multi-query rows (bf16).
@@ -176,6 +180,9 @@ PA_DECLARE_DECODE(launch_decode_f32_d256)
 PA_DECLARE_DECODE(launch_decode_bf16_d64)
 PA_DECLARE_DECODE(launch_decode_bf16_d128)
 PA_DECLARE_DECODE(launch_decode_bf16_d256)
+// bf16 queries over the quantised (E4M3 + scale) cache, head_dim 128 / 256
+PA_DECLARE_DECODE(launch_decode_fp8kv_d128)
+PA_DECLARE_DECODE(launch_decode_fp8kv_d256)
 #undef PA_DECLARE_DECODE
 
 
@@ -234,5 +241,13 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t
                                      void *key_cache, void *value_cache, const int64_t *slots,
                                      int64_t num_tokens, int64_t row_bytes, int64_t num_slots,
                                      cudaStream_t stream);
+
+// reshape_and_cache into the quantised cache (E4M3 codes + a float32 scale per
+// row); key / value are bf16 (elem_bytes 2) or float32 (4), stride in elements.
+cudaError_t launch_quantize_kv_fp8(const void *key, const void *value, int64_t stride,
+                                   int elem_bytes, uint8_t *key_codes, uint8_t *value_codes,
+                                   float *key_scales, float *value_scales, const int64_t *slots,
+                                   int64_t num_tokens, int num_kv_heads, int head_dim,
+                                   int64_t num_slots, cudaStream_t stream);
 
 }  // namespace pa

@@ -147,6 +147,22 @@ class Workload:
             vc[slot // bs, slot % bs] = self.new_v[t]
         return kc, vc
 
+    def all_tokens(self):
+        """Every context token of the batch as one step's input: K and V rows
+        [T, H_kv, D] in request and position order (the prior context read back
+        out of the pool, then this step's new rows) with their slots [T].  A
+        cache in another format (the quantised one) is filled from these, so
+        that it holds the same context as ``key_cache`` after this step."""
+        kc, vc = self.pool_with_new_tokens()
+        bs = self.block_size
+        slots = []
+        for r in range(self.num_seqs):
+            pages = self.block_tables[r]
+            for pos in range(int(self.seq_lens[r])):
+                slots.append(int(pages[pos // bs]) * bs + pos % bs)
+        slots = np.asarray(slots, dtype=np.int64)
+        return kc[slots // bs, slots % bs], vc[slots // bs, slots % bs], slots
+
 
 def _normal(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
     x = rng.standard_normal(size=shape, dtype=np.float32)

@@ -207,3 +207,25 @@ def test_reduce_argument_checks(lib):
     assert f(v(16), v(16), v(16), v(16), v(16), v(16), 2, 4, 256, 4, 96, None, 1, None) == 2
     assert f(v(16), v(16), v(16), v(16), v(16), v(16), 2, 0, 256, 4, 64, None, 1, None) == 1
     assert f(None, v(16), v(16), v(16), v(16), v(16), 2, 4, 256, 4, 64, None, 1, None) == 1
+
+
+def test_quantised_cache_argument_checks(lib):
+    """The quantised-cache calls refuse what they do not take before any CUDA
+    call: head_dim 64, float32 queries, missing scales, a bad dtype."""
+    v = ctypes.c_void_p
+    s = lib.pa_reshape_and_cache_fp8
+    #        key    value   stride codes  codes  kscale vscale slots  T  Hkv D  bs nb dtype
+    assert s(v(16), v(16), 256, v(16), v(16), v(16), v(16), v(16), 0, 2, 128, 16, 8, 1, None) == 0
+    assert s(v(16), v(16), 128, v(16), v(16), v(16), v(16), v(16), 4, 2, 64, 16, 8, 1, None) == 2
+    assert s(v(16), v(16), 128, v(16), v(16), v(16), v(16), v(16), 4, 2, 128, 16, 8, 1, None) == 1
+    assert s(v(16), v(16), 256, v(16), v(16), None, v(16), v(16), 4, 2, 128, 16, 8, 1, None) == 1
+    assert s(v(16), v(16), 256, v(16), v(16), v(16), v(16), v(16), 4, 2, 128, 16, 8, 9, None) == 1
+    a = lib.pa_varlen_attention_fp8kv
+
+    def call(D=128, dtype=1, ks=v(16)):
+        return a(v(16), v(16), v(16), v(16), ks, v(16), v(16), v(16), v(16), 4, 2, 3, 2, 40, 8,
+                 2, D, 16, 8, 0.1, None, 1, 0, None, 0, dtype, None)
+    assert call(D=64) == 2                 # head_dim
+    assert call(dtype=0) == 2              # float32 queries
+    assert call(ks=None) == 1              # missing scales
+    assert "scales" in lib.pa_last_error_string().decode()

@@ -4,9 +4,11 @@ Each case plants one mistake in a copy of oracle/pa_oracle.c -- a wrong GQA
 head map, a causal limit off by one, a wrong slot inside a page, a dropped
 score scale, a sink with the wrong sign, values read from the key cache, a
 split partial whose max is not in the log2 domain, a reduce that forgets the
-exp-sum weights, a scatter into the wrong slot or of padding tokens --
-rebuilds that copy in a temporary tree and runs the pins
-(tests/test_oracle_pins.py) against it: at least one pin must fail.  The
+exp-sum weights, a scatter into the wrong slot or of padding tokens, and in
+the quantised cache a wrong E4M3 exponent bias, ties rounded to odd, a wrong
+quantisation or stored scale, padding tokens quantised -- rebuilds that copy in
+a temporary tree and runs the pins (tests/test_oracle_pins.py,
+tests/test_oracle_fp8.py) against it: at least one pin must fail.  The
 repository's own oracle is not touched.
 """
 import os
@@ -36,8 +38,8 @@ MUTATIONS = [
      "if (a->sinks) den += exp(sink - m);",
      "if (a->sinks) den += exp(-sink - m);"),
     ("values_from_key_cache",
-     "for (int d = 0; d < D; ++d) o[d] += p * elem(a->value_cache, vo + d, a->dtype);",
-     "for (int d = 0; d < D; ++d) o[d] += p * elem(a->key_cache, vo + d, a->dtype);"),
+     "for (int d = 0; d < D; ++d) o[d] += p * elem(a->value_cache, vo + d, a->kv_dtype);",
+     "for (int d = 0; d < D; ++d) o[d] += p * elem(a->key_cache, vo + d, a->kv_dtype);"),
     ("partial_max_natural_units",
      "double t2 = scale * dot * log2e;",
      "double t2 = scale * dot;"),
@@ -48,8 +50,24 @@ MUTATIONS = [
      "int64_t page = slot / block_size, off = slot % block_size;",
      "int64_t page = slot / block_size, off = (slot + 1) % block_size;"),
     ("scatter_padding",
-     "if (slot < 0) continue; /* padding token */",
-     "if (slot < 0) slot = 0;"),
+     "if (slot < 0) continue; /* padding token */\n        if (slot >= num_blocks * block_size) return -1;\n        int64_t page",
+     "if (slot < 0) slot = 0;\n        if (slot >= num_blocks * block_size) return -1;\n        int64_t page"),
+    # the quantised cache (pins in tests/test_oracle_fp8.py)
+    ("e4m3_exponent_bias",
+     "else v = ldexp(1.0 + (double)m / 8.0, e - 7);",
+     "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("e4m3_ties_to_odd",
+     "best = (elo < ehi || (elo == ehi && (lo & 1) == 0)) ? lo : hi;",
+     "best = (elo < ehi || (elo == ehi && (lo & 1) == 1)) ? lo : hi;"),
+    ("quantise_inverse_scale",
+     "const float inv = 448.0f / amax;",
+     "const float inv = 256.0f / amax;"),
+    ("quantise_stored_scale",
+     "scales[slot * num_kv_heads + h] = amax / 448.0f;",
+     "scales[slot * num_kv_heads + h] = amax / 256.0f;"),
+    ("quantise_padding",
+     "if (slot < 0) continue; /* padding token */\n        if (slot >= num_blocks * block_size) return -1;\n        for (int which",
+     "if (slot < 0) slot = 0;\n        if (slot >= num_blocks * block_size) return -1;\n        for (int which"),
 ]
 
 
@@ -63,7 +81,7 @@ def _tree(dst):
         shutil.copy(os.path.join(ROOT, "paged_kv_varlen_gb300", f),
                     os.path.join(dst, "paged_kv_varlen_gb300", f))
     os.makedirs(os.path.join(dst, "tests"))
-    for f in ("conftest.py", "test_oracle_pins.py"):
+    for f in ("conftest.py", "test_oracle_pins.py", "test_oracle_fp8.py"):
         shutil.copy(os.path.join(ROOT, "tests", f), os.path.join(dst, "tests", f))
     shutil.copytree(os.path.join(ROOT, "tests", "golden"), os.path.join(dst, "tests", "golden"))
 
@@ -72,7 +90,7 @@ def _run_pins(tree):
     env = dict(os.environ, PYTHONDONTWRITEBYTECODE="1")
     return subprocess.run(
         [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-         os.path.join("tests", "test_oracle_pins.py")],
+         os.path.join("tests", "test_oracle_pins.py"), os.path.join("tests", "test_oracle_fp8.py")],
         cwd=tree, env=env, capture_output=True, text=True, timeout=600)
 
 
