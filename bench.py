@@ -13,7 +13,11 @@ algorithmic bytes per step / step time.  The default run also times the other
 three workloads of the metric, each in a sub-record of the same JSON line
 (``workloads``: 2 varlen causal prefill -> TFLOP/s; 3 mixed packed step ->
 tokens/s; 4 long-context decode with sinks -> GB/s), each with its own
-roofline, end-to-end figure and CPU baseline.  ``--workload N`` times only N.
+roofline, end-to-end figure and CPU baseline; then the padded layout of the
+prefill batch and the two decode workloads over the quantised KV cache
+(``1_fp8kv``, ``4_fp8kv``: E4M3 codes with a float32 scale per (token, KV
+head) row, bytes counted as read).  ``--workload N`` times only N;
+``--kv-cache fp8 --workload N`` only N over the quantised cache.
 
 Algorithmic work per step: every visible (query row, key) pair costs
 4 * D flops per query head (QK^T and PV); bytes are each context token's K and
@@ -23,7 +27,7 @@ workloads, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload 1..4] [--no-cpu-baseline] [--layout packed|padded]
-                    [--step two-call|fused] [--only-primary]
+                    [--step two-call|fused] [--only-primary] [--kv-cache bf16|fp8]
 
 Under torchrun (N > 1) every rank runs its own independent batch (requests are
 independent units: weak scaling, no collective on the data path); timing is
@@ -556,6 +560,168 @@ def measure(args, widx, rank, world, local, with_cpu_baseline):
     return rec
 
 
+def fp8kv_work(w) -> dict:
+    """Algorithmic work of a step over the quantised cache: every context
+    token's K and V rows once per KV head as D one-byte codes plus a float32
+    scale; bf16 queries and outputs; the quantising scatter reads the new bf16
+    rows and writes their codes and scales."""
+    Hkv, D = w.num_kv_heads, w.head_dim
+    kv = int(w.seq_lens.sum()) * Hkv * (D + 4) * 2
+    qo = 2 * w.total_q * w.num_q_heads * D * 2
+    pages = int(((w.seq_lens + w.block_size - 1) // w.block_size).sum())
+    meta = 4 * pages + 4 * (w.num_seqs * 2 + 1)
+    scatter = 2 * w.total_q * Hkv * (2 * D + D + 4) + 8 * w.total_q
+    flops = 4.0 * D * w.num_q_heads * float(visible_keys(w).sum())
+    return {"kv": kv, "attention_bytes": kv + qo + meta, "step_bytes": kv + qo + meta + scatter,
+            "flops": flops, "tokens": w.total_q}
+
+
+def measure_fp8kv(args, widx, rank, world, local):
+    """Times a decode workload over the quantised KV cache (E4M3 codes with a
+    float32 scale per (token, KV head) row): one step = the quantising scatter
+    of the step's new rows, then attention over the quantised pool.  The pool
+    is quantised once, untimed, from the workload's bf16 pool."""
+    import torch
+    from paged_kv_varlen_gb300 import binding as pa
+    from paged_kv_varlen_gb300 import workloads as wl
+
+    device = torch.device("cuda", local)
+    w = wl.workload(widx)
+    assert workload_kind(w) == "decode" and w.dtype == "bf16"
+    work = fp8kv_work(w)
+    nb, bs, Hkv, D = w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(
+            torch.bfloat16)
+
+    q, nk, nv = dev(w.q), dev(w.new_k), dev(w.new_v)
+    kcodes = torch.empty((nb, bs, Hkv, D), dtype=torch.uint8, device=device)
+    vcodes = torch.empty_like(kcodes)
+    kscales = torch.empty((nb, bs, Hkv), dtype=torch.float32, device=device)
+    vscales = torch.empty_like(kscales)
+    all_slots = torch.arange(nb * bs, dtype=torch.int64, device=device)
+    stream = torch.cuda.current_stream(device)
+    kc = dev(w.key_cache).view(nb * bs, Hkv, D)
+    vc = dev(w.value_cache).view(nb * bs, Hkv, D)
+    pa.pa_reshape_and_cache_fp8(kc, vc, kcodes, vcodes, kscales, vscales, all_slots,
+                                stream=stream)
+    del kc, vc, all_slots
+    sm = torch.from_numpy(w.slot_mapping).to(device)
+    cu = torch.from_numpy(w.cu_seqlens_q).to(device)
+    sl = torch.from_numpy(w.seq_lens_k).to(device)
+    bt = torch.from_numpy(w.block_tables).to(device)
+    sk = torch.from_numpy(w.sinks).to(device) if w.sinks is not None else None
+    out = torch.empty_like(q)
+    P = w.partition_size
+    ws_bytes = pa.pa_varlen_attention_workspace_size(w.num_seqs, w.max_seqlen_k, w.num_q_heads,
+                                                     D, P)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    P_used = pa.pa_choose_partition_size(w.num_seqs, Hkv, w.max_seqlen_k, P, sms)
+    launches_per_step = 2 + (1 if P_used > 0 else 0)
+
+    def step(q_in=q, k_in=nk, v_in=nv, s_in=sm, cu_in=cu, sl_in=sl, bt_in=bt, events=None):
+        pa.pa_reshape_and_cache_fp8(k_in, v_in, kcodes, vcodes, kscales, vscales, s_in,
+                                    stream=stream)
+        if events is not None:
+            events[0].record(stream)
+        pa.pa_varlen_attention_fp8kv(out, q_in, kcodes, vcodes, kscales, vscales, cu_in, sl_in,
+                                     bt_in, max_seqlen_q=w.max_seqlen_q,
+                                     max_seqlen_k=w.max_seqlen_k, scale=w.scale, sinks=sk,
+                                     causal=w.causal, partition_size=P, workspace=ws,
+                                     stream=stream)
+        if events is not None:
+            events[1].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    steps = args.steps
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(gpu_id_for(torch, local))
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.mark_on()
+    start.record(stream)
+    for i in range(steps):
+        step(events=ev[i])
+    end.record(stream)
+    end.synchronize()
+    clocks.mark_off()
+    barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert pa.pa_device_error() == 0, "device error word set during the benchmark"
+    step_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, device) / steps
+    attn_s = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ev) / steps / 1e3, world,
+                            device)
+    value, unit = metric_value("decode", work, step_s, world)
+
+    from paged_kv_varlen_gb300.staging import StepStaging
+    stage = StepStaging({"q": q, "new_k": nk, "new_v": nv, "slot_mapping": sm,
+                         "cu_seqlens_q": cu, "seq_lens_k": sl, "block_tables": bt}, device)
+    for name, t in (("q", q), ("new_k", nk), ("new_v", nv), ("slot_mapping", sm),
+                    ("cu_seqlens_q", cu), ("seq_lens_k", sl), ("block_tables", bt)):
+        stage.host[name].copy_(t.cpu())
+    dv = stage.dev
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        stage.upload()
+        step(dv["q"], dv["new_k"], dv["new_v"], dv["slot_mapping"], dv["cu_seqlens_q"],
+             dv["seq_lens_k"], dv["block_tables"])
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    e1.record(stream)
+    e1.synchronize()
+    barrier()
+    assert pa.pa_device_error() == 0, "device error word set during the end-to-end steps"
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device) / steps
+    e2e_value, _ = metric_value("decode", work, e2e_s, world)
+
+    hbm, _, peak_kind = measured_peaks()
+    achieved = work["attention_bytes"] / attn_s / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": None,
+            "kernel": "paged_decode_kernel (8-bit KV) + split_reduce_kernel (one attention call)",
+            "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                            if peak_kind == "measured" else "fallback"),
+            "avg_launch_us": round(attn_s * 1e6, 3)}
+    cfg = workload_config(w, widx, P_used, "packed",
+                          "pa_reshape_and_cache_fp8 + pa_varlen_attention_fp8kv", world, work,
+                          flushed=False)
+    cfg["kv_cache"] = "E4M3 codes + float32 scale per (token, KV head) row"
+    rec = {"value": round(value, 3), "unit": unit, "ms_per_step": round(1e3 * step_s, 5),
+           "dtype": "bf16 q/out, e4m3 K/V codes, f32 accumulation", "config": cfg,
+           "kv_gbs": round(world * work["step_bytes"] / step_s / 1e9, 2),
+           "tokens_per_s": round(world * w.total_q / step_s, 1), "roofline": roof,
+           "e2e": {"value": round(e2e_value, 3), "unit": unit,
+                   "h2d_bytes_per_step": int(stage.nbytes),
+                   "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size()),
+                   "ms_per_step": round(1e3 * e2e_s, 5)},
+           "gpu_launches": int(launches_per_step * steps), "clocks": clk}
+    del q, nk, nv, kcodes, vcodes, kscales, vscales, out, ws, stage
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args, rank, world, local):
     import torch
     from paged_kv_varlen_gb300 import workloads as wl
@@ -569,6 +735,17 @@ def run_ours(args, rank, world, local):
 
     primary = args.workload or DEFAULT_WORKLOAD
     with_cpu = not args.no_cpu_baseline
+    if args.kv_cache == "fp8":
+        rec = measure_fp8kv(args, primary, rank, world, local)
+        rec.update({"metric": METRIC, "n_gpus": world, "steps": args.steps,
+                    "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                    "vs_baseline": None, "data": "synthetic (seeded N(0,1) Q/K/V)"})
+        if rank == 0:
+            print(json.dumps(rec), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
     line = measure(args, primary, rank, world, local, with_cpu)
     if args.workload is None and not args.only_primary:
         subs = {}
@@ -584,6 +761,9 @@ def run_ours(args, rank, world, local):
         padded_args.steps = min(args.steps, 500)
         rec = measure(padded_args, 2, rank, world, local, False)
         subs["2_padded"] = {k: rec[k] for k in keep if k in rec}
+        # the decode batches over the quantised KV cache
+        for widx in (1, 4):
+            subs[f"{widx}_fp8kv"] = measure_fp8kv(args, widx, rank, world, local)
         line["workloads"] = subs
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -610,7 +790,12 @@ def main(argv=None):
     ap.add_argument("--step", choices=["fused", "two-call"], default="fused",
                     help="fused: one pa_scatter_and_attend call per step; two-call: "
                          "pa_reshape_and_cache then pa_varlen_attention")
+    ap.add_argument("--kv-cache", choices=["bf16", "fp8"], default="bf16",
+                    help="fp8: time only the decode workload (1 or 4) over the quantised "
+                         "cache (E4M3 codes + a float32 scale per row)")
     args = ap.parse_args(argv)
+    if args.kv_cache == "fp8" and (args.workload or DEFAULT_WORKLOAD) not in (1, 4):
+        ap.error("--kv-cache fp8 times the decode workloads 1 and 4 only")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
