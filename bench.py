@@ -700,7 +700,7 @@ def measure_fp8kv(args, widx, rank, world, local):
     achieved = work["attention_bytes"] / attn_s / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "traffic": None,
-            "kernel": "paged_decode_kernel (8-bit KV) + split_reduce_kernel (one attention call)",
+            "kernel": "paged_decode_tc_fp8_kernel + split_reduce_kernel (one attention call)",
             "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                             if peak_kind == "measured" else "fallback"),
             "avg_launch_us": round(attn_s * 1e6, 3)}

@@ -222,10 +222,13 @@ pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t k
  * the same packed rows, masking, sinks, split-KV plan, workspace (sized by
  * pa_varlen_attention_workspace_size) and result, with every key and value
  * row taken as value(code) * scale.  q and out are bf16 (`dtype` must be
- * PA_BF16).  The arithmetic is float32 on the CUDA cores (single-query rows
- * split over partitions and merged by the shared reduce, multi-query rows one
- * CTA per row and KV head).  Returns the statuses of pa_varlen_attention, and
- * PA_ERR_UNSUPPORTED for another dtype or head_dim.
+ * PA_BF16).  Single-query rows run on the tensor cores (a persistent kernel:
+ * QK^T as an E4M3 MMA on the codes with the queries split exactly into two
+ * E4M3 parts, PV in f16 from V codes converted exactly, fp32 accumulation;
+ * split over partitions and merged by the shared reduce); multi-query rows on
+ * the CUDA cores in float32, one CTA per row and KV head.  Returns the
+ * statuses of pa_varlen_attention, and PA_ERR_UNSUPPORTED for another dtype
+ * or head_dim.
  */
 pa_status pa_varlen_attention_fp8kv(
     void *out, const void *q, const void *key_codes, const void *value_codes,

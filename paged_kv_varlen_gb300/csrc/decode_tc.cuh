@@ -271,6 +271,234 @@ __device__ __forceinline__ int64_t dtc_block_scan(int64_t v, long long *scratch,
     return x + before;
 }
 
+// Shared-memory records of a CTA's share of the batch: written by
+// dtc_plan_share, read by dtc_first_item.
+struct DtcPlanSmem {
+    int *lens_cu;         // [NT + 1] cu_seqlens_q when num_seqs <= NT
+    int *lens_sl;         // [NT] seq_lens_k when num_seqs <= NT
+    int *plan_rk;         // [4] first item (request, index); cut item (request, index)
+    long long *plan_s;    // [2] s_lo, s_hi
+    int *plan_j;          // [2] j_lo, j_hi
+    long long *scratch;   // [NT / 32] block-scan scratch
+};
+
+// Every thread of the CTA (NT threads) calls it; the records in `ps` are
+// complete after the CTA's next __syncthreads.  Expects ps.plan_rk[0] = S,
+// plan_rk[1] = 0, plan_rk[2] = -1, plan_rk[3] = 0, plan_s = {0, INT64_MAX},
+// plan_j = {0, 0} set before the call.
+template <int NT>
+__device__ __forceinline__ void dtc_plan_share(const DecodeTcArgs &a, const DtcPlanSmem &ps) {
+    const int tid = threadIdx.x;
+    const int S = a.num_seqs;
+    const int hkv = a.num_kv_heads;
+    int *lens_cu = ps.lens_cu;
+    int *lens_sl = ps.lens_sl;
+    int *plan_rk = ps.plan_rk;
+    long long *plan_s = ps.plan_s;
+    int *plan_j = ps.plan_j;
+    long long *scratch = ps.scratch;
+    // ---- this CTA's share [lo, hi) of the batch's cumulative work, cut at
+    // tile boundaries (see dtc_cut): the request containing lo (resp. hi)
+    // records where the share starts (ends).  With at most THREADS requests
+    // one pass suffices: thread r reads request r's lengths once (kept in
+    // shared memory for the iterators), one block scan gives every request's
+    // cumulative work and the total.
+    const bool one_pass = S <= NT;
+    const bool split = a.partition_size > 0;
+    {
+        int64_t acc = 0;
+        DtcReq q1 = {0, 0, 0, 0, 0};
+        if (one_pass) {
+            if (tid < S) {
+                const int c0 = a.cu_seqlens_q[tid], c1 = a.cu_seqlens_q[tid + 1];
+                const int sl = a.seq_lens_k[tid];
+                lens_cu[tid] = c0;
+                lens_sl[tid] = sl;
+                if (tid == S - 1) lens_cu[S] = c1;
+                q1 = dtc_request_from(a, c0, c1, sl);
+                acc = dtc_work(q1, hkv);
+            }
+        } else {
+            for (int r = tid; r < S; r += NT) acc += dtc_work(dtc_request(a, r), hkv);
+        }
+        int64_t W;
+        const int64_t incl = dtc_block_scan<NT>(acc, scratch, &W);   // (orders setup writes)
+        const int64_t nb = gridDim.x, b = blockIdx.x;
+        const int64_t lo = (W / nb) * b + (W % nb) * b / nb;
+        const int64_t hi = (W / nb) * (b + 1) + (W % nb) * (b + 1) / nb;
+        // Items are cut between CTAs only when a share holds fewer than ten
+        // full-partition items: whole items then leave the shares up to ~5 %
+        // apart, while a cut starts the next CTA mid-item, out of step with
+        // the others' item boundaries -- measured on GB300 to cost ~8 % of a
+        // GQA decode batch of 4-tile items, and to gain ~3.5 % on a batch of
+        // 8-tile items at 8 items per CTA.
+        const bool cut_items =
+            split && W / nb < 10 * (5 * (int64_t)((a.partition_size + 127) / 128) + 3);
+        // request r (cumulative work E, total w) containing lo or hi; the one
+        // containing lo also warms L2 with the block-table entries of the first
+        // tiles (the producers fetch them next)
+        auto boundaries = [&](int r, const DtcReq &q, int64_t E, int64_t w) {
+            if (q.items == 0 || lo >= hi) return;
+            if (E <= lo && lo < E + w) {
+                int j;
+                int64_t st;
+                const int k = dtc_cut(q, hkv, cut_items, lo - E, &j, &st);
+                plan_rk[0] = r;
+                plan_rk[1] = k;
+                plan_s[0] = E + st;
+                plan_j[0] = j;
+                if (k < q.items) {
+                    const int kt0 = (split ? (k / hkv) * a.partition_size : 0) + j * 128;
+                    const int b0 = kt0 / a.block_size;   // < max_blocks_per_seq: keys there
+                    const int32_t *bt = a.block_tables + (int64_t)r * a.max_blocks_per_seq + b0;
+                    prefetch_l2(bt);
+                    if (b0 + 32 < a.max_blocks_per_seq) prefetch_l2(bt + 32);
+                }
+            }
+            if (E <= hi && hi < E + w) {
+                int j;
+                int64_t st;
+                const int k = dtc_cut(q, hkv, cut_items, hi - E, &j, &st);
+                plan_s[1] = E + st;
+                plan_j[1] = j;
+                if (j > 0) {
+                    plan_rk[2] = r;
+                    plan_rk[3] = k;
+                }
+            }
+        };
+        if (one_pass) {
+            if (tid < S) boundaries(tid, q1, incl - acc, acc);
+        } else {
+            int64_t carry = 0;
+            for (int base = 0; base < S && lo < hi && carry <= hi; base += NT) {
+                const int r = base + tid;
+                const DtcReq q = r < S ? dtc_request(a, r) : DtcReq{0, 0, 0, 0, 0};
+                const int64_t w = dtc_work(q, hkv);
+                int64_t tot;
+                const int64_t E = carry + dtc_block_scan<NT>(w, scratch, &tot) - w;
+                if (r < S) boundaries(r, q, E, w);
+                carry += tot;
+            }
+        }
+    }
+}
+
+// The CTA's first item and the bounds of its share (after dtc_plan_share and a
+// __syncthreads); thread 0 records the item cut at the share's end in the cut
+// table.  Returns an iterator with r == num_seqs when the share holds no tile.
+template <int NT>
+__device__ __forceinline__ DtcIter dtc_first_item(const DecodeTcArgs &a, const DtcPlanSmem &ps,
+                                                  DtcCut *cut_out, int64_t *range_end) {
+    const int tid = threadIdx.x;
+    const int S = a.num_seqs;
+    const int hkv = a.num_kv_heads;
+    const bool one_pass = S <= NT;
+    const bool split = a.partition_size > 0;
+    const int *lens_cu = ps.lens_cu;
+    const int *lens_sl = ps.lens_sl;
+    const int *plan_rk = ps.plan_rk;
+    const long long *plan_s = ps.plan_s;
+    const int *plan_j = ps.plan_j;
+    DtcCut &cut = *cut_out;
+    cut.s_lo = plan_s[0];
+    cut.s_hi = plan_s[1];
+    cut.j_lo = plan_j[0];
+    cut.j_hi = plan_j[1];
+    // items: from (s_lo, tile j_lo) up to (s_hi, tile j_hi)
+    *range_end = cut.s_hi + (cut.j_hi > 0 ? 1 : 0);
+    DtcIter it0;
+    it0.r = plan_rk[0];
+    it0.k = plan_rk[1];
+    it0.s = cut.s_lo;
+    const bool has_work =
+        it0.r < S && (cut.s_lo < cut.s_hi || (cut.s_lo == cut.s_hi && cut.j_lo < cut.j_hi));
+    if (!has_work) it0.r = S;
+    if (it0.r < S) {
+        const int r = it0.r;
+        if (one_pass) {   // the lengths of this request and the next one from shared memory
+            dtc_enter_from(a, it0, r, lens_cu[r], lens_cu[r + 1], lens_sl[r],
+                           r + 1 < S ? lens_cu[r + 2] : 0, r + 1 < S ? lens_sl[r + 1] : 0);
+        } else {
+            dtc_enter(a, it0, r, a.cu_seqlens_q[r], a.cu_seqlens_q[r + 1], a.seq_lens_k[r]);
+        }
+        if (it0.k >= it0.q.items) {   // the share starts with the next request
+            it0.k = it0.q.items - 1;
+            it0.s -= it0.q.wlast;   // (dtc_next adds the last item's weight back)
+            dtc_next(a, it0, cut);
+        } else {
+            dtc_fill(a, it0, cut);
+        }
+    }
+    // the table of items cut at a share's end (their first part's partial is
+    // in the CTA's extra slot; the reduce merges it).  A CTA whose share holds
+    // no tile writes no partial and records none.
+    if (split && a.cut_tab != nullptr && tid == 0) {
+        const int cr = plan_rk[2], ck = plan_rk[3];
+        a.cut_tab[blockIdx.x] = has_work && cr >= 0 ? make_int4(cr, ck % hkv, ck / hkv, 0)
+                                                    : make_int4(-1, 0, 0, 0);
+    }
+    return it0;
+}
+
+// Writes an item's result for query heads h * G .. h * G + G - 1 from the
+// thread of TMEM lane t (dims t, t + 128, ...): with split partials, the
+// normalised partial, exp-sum and reference max (the first part of an item cut
+// at the share's end into the CTA's extra slot); otherwise the output rows,
+// with the sink in the denominator.
+template <int D, int G>
+__device__ __forceinline__ void dtc_store_item(const DecodeTcArgs &a, const DtcIter &cur,
+                                               const DtcCut &cut, int t,
+                                               const float (&o)[D / 128][8], const float (&L)[G],
+                                               const float (&m_ref)[G]) {
+    using C = DtcCfg<D>;
+    const bool split = a.partition_size > 0;
+    const int Hq = a.num_q_heads;
+    const int hq0 = cur.h * G;
+    if (split) {
+        // the first part of an item cut at the share's end goes to the
+        // CTA's extra slot, every other partial to its partition's slot
+        const bool tail = cur.s == cut.s_hi && cut.j_hi > 0;
+        const int64_t slot0 =
+            tail ? (int64_t)blockIdx.x * G
+                 : ((int64_t)cur.r * a.max_parts + cur.p) * Hq + hq0;
+        float *po = tail ? a.xpart_o : a.part_o;
+        float *pm = tail ? a.xpart_m : a.part_m;
+        float *pl = tail ? a.xpart_l : a.part_l;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float inv = L[g] > 0.f ? 1.f / L[g] : 0.f;
+#pragma unroll
+            for (int c = 0; c < C::KS; ++c)
+                po[(slot0 + g) * D + c * 128 + t] = o[c][g] * inv;
+            if (t == g) {
+                pm[slot0 + g] = m_ref[g];
+                pl[slot0 + g] = L[g];
+            }
+        }
+    } else {
+        __nv_bfloat16 *orow =
+            reinterpret_cast<__nv_bfloat16 *>(a.out) + (cur.row * Hq + hq0) * D;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float sc = 0.f;
+            if (L[g] > 0.f) {
+                if (a.sinks) {
+                    const float sk2 = a.sinks[hq0 + g] * kLog2e;
+                    const float M2 = fmaxf(m_ref[g], sk2);
+                    const float f = exp2f(m_ref[g] - M2);
+                    sc = f / (L[g] * f + exp2f(sk2 - M2));
+                } else {
+                    sc = 1.f / L[g];
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < C::KS; ++c)
+                orow[g * D + c * 128 + t] = __float2bfloat16_rn(o[c][g] * sc);
+        }
+    }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(288, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
@@ -360,133 +588,16 @@ __global__ void __launch_bounds__(288, 1)
     // kernel is this step's scatter)
     if (!a.after_scatter) pdl_wait();
 
-    // ---- this CTA's share [lo, hi) of the batch's cumulative work, cut at
-    // tile boundaries (see dtc_cut): the request containing lo (resp. hi)
-    // records where the share starts (ends).  With at most THREADS requests
-    // one pass suffices: thread r reads request r's lengths once (kept in
-    // shared memory for the iterators), one block scan gives every request's
-    // cumulative work and the total.
-    const bool one_pass = S <= C::THREADS;
+    const DtcPlanSmem ps = {lens_cu, lens_sl, plan_rk, plan_s, plan_j, scratch};
+    dtc_plan_share<C::THREADS>(a, ps);
     const bool split = a.partition_size > 0;
-    {
-        int64_t acc = 0;
-        DtcReq q1 = {0, 0, 0, 0, 0};
-        if (one_pass) {
-            if (tid < S) {
-                const int c0 = a.cu_seqlens_q[tid], c1 = a.cu_seqlens_q[tid + 1];
-                const int sl = a.seq_lens_k[tid];
-                lens_cu[tid] = c0;
-                lens_sl[tid] = sl;
-                if (tid == S - 1) lens_cu[S] = c1;
-                q1 = dtc_request_from(a, c0, c1, sl);
-                acc = dtc_work(q1, hkv);
-            }
-        } else {
-            for (int r = tid; r < S; r += C::THREADS) acc += dtc_work(dtc_request(a, r), hkv);
-        }
-        int64_t W;
-        const int64_t incl = dtc_block_scan<C::THREADS>(acc, scratch, &W);   // (orders setup writes)
-        const int64_t nb = gridDim.x, b = blockIdx.x;
-        const int64_t lo = (W / nb) * b + (W % nb) * b / nb;
-        const int64_t hi = (W / nb) * (b + 1) + (W % nb) * (b + 1) / nb;
-        // Items are cut between CTAs only when a share holds fewer than ten
-        // full-partition items: whole items then leave the shares up to ~5 %
-        // apart, while a cut starts the next CTA mid-item, out of step with
-        // the others' item boundaries -- measured on GB300 to cost ~8 % of a
-        // GQA decode batch of 4-tile items, and to gain ~3.5 % on a batch of
-        // 8-tile items at 8 items per CTA.
-        const bool cut_items =
-            split && W / nb < 10 * (5 * (int64_t)((a.partition_size + 127) / 128) + 3);
-        // request r (cumulative work E, total w) containing lo or hi; the one
-        // containing lo also warms L2 with the block-table entries of the first
-        // tiles (the producers fetch them next)
-        auto boundaries = [&](int r, const DtcReq &q, int64_t E, int64_t w) {
-            if (q.items == 0 || lo >= hi) return;
-            if (E <= lo && lo < E + w) {
-                int j;
-                int64_t st;
-                const int k = dtc_cut(q, hkv, cut_items, lo - E, &j, &st);
-                plan_rk[0] = r;
-                plan_rk[1] = k;
-                plan_s[0] = E + st;
-                plan_j[0] = j;
-                if (k < q.items) {
-                    const int kt0 = (split ? (k / hkv) * a.partition_size : 0) + j * 128;
-                    const int b0 = kt0 / a.block_size;   // < max_blocks_per_seq: keys there
-                    const int32_t *bt = a.block_tables + (int64_t)r * a.max_blocks_per_seq + b0;
-                    prefetch_l2(bt);
-                    if (b0 + 32 < a.max_blocks_per_seq) prefetch_l2(bt + 32);
-                }
-            }
-            if (E <= hi && hi < E + w) {
-                int j;
-                int64_t st;
-                const int k = dtc_cut(q, hkv, cut_items, hi - E, &j, &st);
-                plan_s[1] = E + st;
-                plan_j[1] = j;
-                if (j > 0) {
-                    plan_rk[2] = r;
-                    plan_rk[3] = k;
-                }
-            }
-        };
-        if (one_pass) {
-            if (tid < S) boundaries(tid, q1, incl - acc, acc);
-        } else {
-            int64_t carry = 0;
-            for (int base = 0; base < S && lo < hi && carry <= hi; base += C::THREADS) {
-                const int r = base + tid;
-                const DtcReq q = r < S ? dtc_request(a, r) : DtcReq{0, 0, 0, 0, 0};
-                const int64_t w = dtc_work(q, hkv);
-                int64_t tot;
-                const int64_t E = carry + dtc_block_scan<C::THREADS>(w, scratch, &tot) - w;
-                if (r < S) boundaries(r, q, E, w);
-                carry += tot;
-            }
-        }
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     DtcCut cut;
-    cut.s_lo = plan_s[0];
-    cut.s_hi = plan_s[1];
-    cut.j_lo = plan_j[0];
-    cut.j_hi = plan_j[1];
-    // items: from (s_lo, tile j_lo) up to (s_hi, tile j_hi)
-    const int64_t range_end = cut.s_hi + (cut.j_hi > 0 ? 1 : 0);
-    DtcIter it0;
-    it0.r = plan_rk[0];
-    it0.k = plan_rk[1];
-    it0.s = cut.s_lo;
-    const bool has_work =
-        it0.r < S && (cut.s_lo < cut.s_hi || (cut.s_lo == cut.s_hi && cut.j_lo < cut.j_hi));
-    if (!has_work) it0.r = S;
-    if (it0.r < S) {
-        const int r = it0.r;
-        if (one_pass) {   // the lengths of this request and the next one from shared memory
-            dtc_enter_from(a, it0, r, lens_cu[r], lens_cu[r + 1], lens_sl[r],
-                           r + 1 < S ? lens_cu[r + 2] : 0, r + 1 < S ? lens_sl[r + 1] : 0);
-        } else {
-            dtc_enter(a, it0, r, a.cu_seqlens_q[r], a.cu_seqlens_q[r + 1], a.seq_lens_k[r]);
-        }
-        if (it0.k >= it0.q.items) {   // the share starts with the next request
-            it0.k = it0.q.items - 1;
-            it0.s -= it0.q.wlast;   // (dtc_next adds the last item's weight back)
-            dtc_next(a, it0, cut);
-        } else {
-            dtc_fill(a, it0, cut);
-        }
-    }
-    // the table of items cut at a share's end (their first part's partial is
-    // in the CTA's extra slot; the reduce merges it).  A CTA whose share holds
-    // no tile writes no partial and records none.
-    if (split && a.cut_tab != nullptr && tid == 0) {
-        const int cr = plan_rk[2], ck = plan_rk[3];
-        a.cut_tab[blockIdx.x] = has_work && cr >= 0 ? make_int4(cr, ck % hkv, ck / hkv, 0)
-                                                    : make_int4(-1, 0, 0, 0);
-    }
+    int64_t range_end;
+    const DtcIter it0 = dtc_first_item<C::THREADS>(a, ps, &cut, &range_end);
     auto valid = [&](const DtcIter &x) { return x.r < S && x.s < range_end; };
 
     // one tile forward along the sequence; itx counts the non-empty items left
@@ -856,49 +967,7 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) o[c][e] = 0.f;
             }
-            const int hq0 = cur.h * G;
-            if (split) {
-                // the first part of an item cut at the share's end goes to the
-                // CTA's extra slot, every other partial to its partition's slot
-                const bool tail = cur.s == cut.s_hi && cut.j_hi > 0;
-                const int64_t slot0 =
-                    tail ? (int64_t)blockIdx.x * G
-                         : ((int64_t)cur.r * a.max_parts + cur.p) * Hq + hq0;
-                float *po = tail ? a.xpart_o : a.part_o;
-                float *pm = tail ? a.xpart_m : a.part_m;
-                float *pl = tail ? a.xpart_l : a.part_l;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float inv = L[g] > 0.f ? 1.f / L[g] : 0.f;
-#pragma unroll
-                    for (int c = 0; c < C::KS; ++c)
-                        po[(slot0 + g) * D + c * 128 + t] = o[c][g] * inv;
-                    if (t == g) {
-                        pm[slot0 + g] = m_ref[g];
-                        pl[slot0 + g] = L[g];
-                    }
-                }
-            } else {
-                __nv_bfloat16 *orow =
-                    reinterpret_cast<__nv_bfloat16 *>(a.out) + (cur.row * Hq + hq0) * D;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float sc = 0.f;
-                    if (L[g] > 0.f) {
-                        if (a.sinks) {
-                            const float sk2 = a.sinks[hq0 + g] * kLog2e;
-                            const float M2 = fmaxf(m_ref[g], sk2);
-                            const float f = exp2f(m_ref[g] - M2);
-                            sc = f / (L[g] * f + exp2f(sk2 - M2));
-                        } else {
-                            sc = 1.f / L[g];
-                        }
-                    }
-#pragma unroll
-                    for (int c = 0; c < C::KS; ++c)
-                        orow[g * D + c * 128 + t] = __float2bfloat16_rn(o[c][g] * sc);
-                }
-            }
+            dtc_store_item<D, G>(a, cur, cut, t, o, L, m_ref);
             if (cur.ntiles > 0) ++itn;
             ++ie;
             dtc_next(a, cur, cut);

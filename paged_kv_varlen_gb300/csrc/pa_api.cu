@@ -194,7 +194,8 @@ PA_API const char *pa_last_error_string(void) { return g_last_error; }
 
 PA_API const char *pa_build_info(void) {
     return "libpa paged varlen attention; sm_103a; kernels: reshape_and_cache, "
-           "paged_decode_tc (tcgen05/TMEM, persistent), paged_decode (TMA ring, CUDA cores), "
+           "paged_decode_tc (tcgen05/TMEM, persistent), paged_decode_tc_fp8 (E4M3 cache, "
+           "tcgen05), paged_decode (TMA ring, CUDA cores), "
            "paged_prefill_tc (tcgen05/TMEM), split_reduce";
 }
 
@@ -452,6 +453,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
                             num_blocks * block_size, dbox);
         if (st != PA_OK) return st;
         DecodeTcArgs da;
+        memset(&da, 0, sizeof da);
         da.out = out;
         da.cu_seqlens_q = cu_seqlens_q;
         da.seq_lens_k = seq_lens_k;
@@ -793,6 +795,8 @@ PA_API pa_status pa_varlen_attention_fp8kv(
         return PA_ERR_UNSUPPORTED;
     }
     float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
+    float *xpart_o = nullptr, *xpart_m = nullptr, *xpart_l = nullptr;
+    int4 *cut_tab = nullptr;
     if (P > 0) {
         const size_t plan_sz = align256(plan_bytes(num_seqs));
         const SplitLayout L = split_layout(num_seqs, max_parts, num_q_heads, head_dim);
@@ -809,6 +813,11 @@ PA_API pa_status pa_varlen_attention_fp8kv(
         part_o = reinterpret_cast<float *>(w);
         part_m = reinterpret_cast<float *>(w + L.o_bytes);
         part_l = reinterpret_cast<float *>(w + L.o_bytes + L.ml_bytes);
+        w += L.o_bytes + 2 * L.ml_bytes;
+        xpart_o = reinterpret_cast<float *>(w);
+        xpart_m = reinterpret_cast<float *>(w + L.xo_bytes);
+        xpart_l = reinterpret_cast<float *>(w + L.xo_bytes + L.xml_bytes);
+        cut_tab = reinterpret_cast<int4 *>(w + L.xo_bytes + 2 * L.xml_bytes);
     }
 
     const int box_rows = gcd_int(decode_tile_keys(1, head_dim), block_size);
@@ -849,10 +858,52 @@ PA_API pa_status pa_varlen_attention_fp8kv(
         return head_dim == 128 ? launch_decode_fp8kv_d128(group, kmap, vmap, a, grid, s)
                                : launch_decode_fp8kv_d256(group, kmap, vmap, a, grid, s);
     };
-    // single-query rows: one CTA per (partition, KV head, request)
-    a.mode = 0;
-    cudaError_t ce = launch(dim3(max_parts, num_kv_heads, num_seqs));
-    if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode (quantised) launch");
+    // single-query rows: the persistent tensor-core kernel, one CTA per SM
+    // sharing the batch's (request, KV head, partition) items
+    const int dbox = gcd_int(gcd_int(128, block_size), P > 0 ? P : 128);
+    CUtensorMap qmap_d, kmap_d, vmap_d;
+    st = make_query_map(&qmap_d, q, head_dim, num_q_heads, total_q, group, 1);
+    if (st != PA_OK) return st;
+    st = make_code_map(&kmap_d, key_codes, head_dim, num_kv_heads, num_blocks * block_size, dbox);
+    if (st != PA_OK) return st;
+    st = make_code_map(&vmap_d, value_codes, head_dim, num_kv_heads, num_blocks * block_size,
+                       dbox);
+    if (st != PA_OK) return st;
+    DecodeTcArgs da;
+    memset(&da, 0, sizeof da);
+    da.out = out;
+    da.cu_seqlens_q = cu_seqlens_q;
+    da.seq_lens_k = seq_lens_k;
+    da.block_tables = block_tables;
+    da.max_blocks_per_seq = max_blocks_per_seq;
+    da.num_seqs = num_seqs;
+    da.num_q_heads = num_q_heads;
+    da.num_kv_heads = num_kv_heads;
+    da.block_size = block_size;
+    da.qscale = scale * kLog2e;
+    da.sinks = sinks;
+    da.partition_size = P;
+    da.max_parts = max_parts;
+    da.part_o = part_o;
+    da.part_m = part_m;
+    da.part_l = part_l;
+    da.box_rows = dbox;
+    da.err = dev.err;
+    da.after_scatter = 0;
+    da.xpart_o = xpart_o;
+    da.xpart_m = xpart_m;
+    da.xpart_l = xpart_l;
+    da.cut_tab = cut_tab;
+    da.k_scales = key_scales;
+    da.v_scales = value_scales;
+    da.num_blocks = num_blocks;
+    const int64_t items_max = (int64_t)num_seqs * num_kv_heads * max_parts;
+    const int grid = (int)std::min<int64_t>(
+        std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, kMaxDecodeCtas), items_max);
+    cudaError_t ce =
+        head_dim == 128 ? launch_decode_tc_fp8_d128(group, qmap_d, kmap_d, vmap_d, da, grid, s)
+                        : launch_decode_tc_fp8_d256(group, qmap_d, kmap_d, vmap_d, da, grid, s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode_tc (quantised) launch");
     // rows of multi-query requests: one CTA per (row, KV head)
     if (max_seqlen_q > 1) {
         a.mode = 1;
@@ -874,7 +925,11 @@ PA_API pa_status pa_varlen_attention_fp8kv(
         ra.num_q_heads = num_q_heads;
         ra.sinks = sinks;
         ra.meta_before_wait = 1;   // the kernels before it write only out / partials
-        ra.ncut = 0;
+        ra.xpart_o = xpart_o;
+        ra.xpart_m = xpart_m;
+        ra.xpart_l = xpart_l;
+        ra.cut_tab = cut_tab;
+        ra.ncut = grid;
         ra.group = group;
         ce = launch_reduce(2, head_dim, ra, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "split_reduce launch");

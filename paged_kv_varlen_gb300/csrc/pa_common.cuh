@@ -83,6 +83,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *er
     }
 }
 
+// mbar_wait with the retry loop out of line (one shared copy per kernel), for
+// kernels whose many wait sites would otherwise each carry a copy of it.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int *err,
+                                                  volatile int *abort_flag) {
+    return mbar_wait(bar, parity, err, abort_flag);
+}
+__device__ __forceinline__ bool mbar_wait_ool(uint32_t bar, uint32_t parity, int *err,
+                                              volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err, abort_flag);
+}
+
 // Bounded wait that ignores the abort flag (used to drain copies in flight
 // before a CTA exits); gives up silently after `limit` cycles.
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, long long limit) {

@@ -117,6 +117,12 @@ struct DecodeTcArgs {
     // rows (it writes nothing else the kernel reads): only the K/V loads wait
     // for it.  0: the whole kernel waits for the previous kernel first.
     int after_scatter;
+    // quantised cache only: float32 scale of each (slot, KV head)'s K and V
+    // row, [num_blocks * block_size, H_kv], and the pool's pages (page ids at
+    // or past it give a zero scale); nullptr / 0 for a bf16 cache
+    const float *k_scales;
+    const float *v_scales;
+    int64_t num_blocks;
 };
 
 // Keys per K/V tile of the multi-query kernel, keys of one V sub-tile (the
@@ -230,6 +236,9 @@ PA_DECLARE_TC(launch_prefill_tc_d256)
                      cudaStream_t stream);
 PA_DECLARE_DTC(launch_decode_tc_d128)
 PA_DECLARE_DTC(launch_decode_tc_d256)
+// the same over the quantised cache (E4M3 codes + float32 row scales)
+PA_DECLARE_DTC(launch_decode_tc_fp8_d128)
+PA_DECLARE_DTC(launch_decode_tc_fp8_d256)
 #undef PA_DECLARE_DTC
 
 cudaError_t launch_reduce(int elem_bytes, int head_dim, const ReduceArgs &a, cudaStream_t stream);

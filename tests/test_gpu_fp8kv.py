@@ -148,3 +148,47 @@ def test_fp8kv_full_size_decode_batch():
     pools = QuantPools(w)
     pools.check_bits()
     pools.attention(partition_size=w.partition_size)
+
+
+@pytest.mark.parametrize("max_q", [1, 6])
+def test_fp8kv_subnormal_codes(max_q):
+    """Rows whose codes are E4M3 subnormals (+-m * 2^-9, m = 0..7) except one
+    code of 448 in dim 0, with scale 16: the subnormal dims hold values of
+    +-1/32 .. 7/32.  K and V share the codes and the softmax scale is 1, so
+    the queries (zero in dim 0) score the keys by their subnormal dims alone
+    and the output's dims 1.. are a query-weighted mean of them: about 0.045
+    on average, against an error of the same size if either K or V lost its
+    subnormals (flushed to zero by the decoder or the tensor cores).  Dim 0
+    of the output (7168) is compared relative to its size."""
+    w = wl.random_small(391 + max_q, dtype=wl.BF16, num_seqs=6, num_q_heads=8, num_kv_heads=2,
+                        head_dim=128, max_prior=700, max_q=max_q)
+    nb, bs, Hkv, D = w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim
+    rng = np.random.default_rng(7)
+    sub = rng.integers(0, 8, size=(1, nb, bs, Hkv, D)).astype(np.uint8)     # 0 .. 7 x 2^-9
+    sub |= (rng.integers(0, 2, size=sub.shape) << 7).astype(np.uint8)      # random sign
+    sub[..., 0] = 0x7E                                                      # 448
+    kc = vc = sub[0]
+    scales = np.full((nb, bs, Hkv), 16.0, np.float32)
+    qf = rng.normal(0, 2, size=(w.total_q, w.num_q_heads, D)).astype(np.float32)
+    qf[..., 0] = 0
+    q_bits = (qf.view(np.uint32) >> 16).astype(np.uint16)                  # exact in bf16 by truncation
+    q = to_dev(q_bits, wl.BF16)
+    out = torch.full_like(q, float("nan"))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()       # noqa: E731
+    pa.pa_varlen_attention_fp8kv(out, q, dev(kc), dev(vc), dev(scales), dev(scales),
+                                 dev(w.cu_seqlens_q), dev(w.seq_lens_k), dev(w.block_tables),
+                                 max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k,
+                                 scale=1.0, causal=w.causal, partition_size=-1)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    ref = orc.paged_attention_kv(q_bits, orc.dequantize_kv_fp8(kc, scales),
+                                 orc.dequantize_kv_fp8(vc, scales), w.cu_seqlens_q,
+                                 w.seq_lens_k, w.block_tables, q_dtype=wl.BF16,
+                                 num_q_heads=w.num_q_heads, num_kv_heads=Hkv, head_dim=D,
+                                 block_size=bs, scale=1.0, causal=w.causal)
+    got = from_dev(out)
+    # the subnormal dims carry the test: their outputs are far from zero
+    assert np.abs(ref[..., 1:]).mean() > 0.02
+    assert_close(got[..., 1:], ref[..., 1:], wl.BF16, f"fp8 subnormal codes q<={max_q}")
+    rel = np.abs(got[..., 0] - ref[..., 0]) / np.maximum(np.abs(ref[..., 0]), 1.0)
+    assert rel.max() <= 1e-2
