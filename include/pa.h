@@ -61,6 +61,32 @@ const char *pa_last_error_string(void);
 const char *pa_build_info(void);
 
 /*
+ * Launch plans (the kwkr.cn hands-on section's dispatch diagnostics: which
+ * kernel served the call and with which partition size).
+ *
+ * pa_describe_plan -- host only, no device call: writes into buf (buf_len
+ * bytes, NUL-terminated, truncated if short) the launches that
+ * pa_varlen_attention (quantised = 0) or pa_varlen_attention_fp8kv
+ * (quantised = 1) makes for these sizes on a GPU of sm_count SMs, as one
+ * line of key=value pairs: dtype, cache (plain / e4m3), head_dim, group,
+ * partition (split-KV partition used, 0 = none), max_parts, decode_kernel
+ * and decode_grid (single-query rows), mq_kernel and mq_grid (rows of
+ * multi-query requests; none when max_seqlen_q <= 1), reduce and
+ * reduce_grid, workspace (bytes the call needs; 0 = none).  Returns
+ * PA_ERR_INVALID_ARG for a null buffer or impossible sizes.
+ *
+ * pa_last_plan -- the same line for the last attention call this thread
+ * launched ("none" before the first); static per-thread buffer.  With the
+ * environment variable PA_DEBUG set (not "0") every attention call also
+ * prints its line to stderr, prefixed "pa: ".
+ */
+pa_status pa_describe_plan(int num_seqs, int64_t total_q, int max_seqlen_q, int max_seqlen_k,
+                           int num_q_heads, int num_kv_heads, int head_dim, int partition_size,
+                           pa_dtype dtype, int quantised, int sm_count, char *buf,
+                           size_t buf_len);
+const char *pa_last_plan(void);
+
+/*
  * pa_reshape_and_cache -- scatter this step's K/V rows into the page pool.
  * (kwkr.cn kernel table: reshape_and_cache writes projected K/V into the
  * paged cache.)

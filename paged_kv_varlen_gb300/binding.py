@@ -45,6 +45,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pa_last_error_string.argtypes = []
     lib.pa_build_info.restype = ctypes.c_char_p
     lib.pa_build_info.argtypes = []
+    lib.pa_describe_plan.restype = I
+    lib.pa_describe_plan.argtypes = [I, L, I, I, I, I, I, I, I, I, I, ctypes.c_char_p, S]
+    lib.pa_last_plan.restype = ctypes.c_char_p
+    lib.pa_last_plan.argtypes = []
     lib.pa_reshape_and_cache.restype = I
     lib.pa_reshape_and_cache.argtypes = [P, P, L, P, P, P, L, I, I, I, L, I, P]
     lib.pa_varlen_attention.restype = I
@@ -127,6 +131,32 @@ def pa_varlen_attention_workspace_size(num_seqs: int, max_seqlen_k: int, num_q_h
                                        head_dim: int, partition_size: int = 0) -> int:
     return int(load_library().pa_varlen_attention_workspace_size(
         num_seqs, max_seqlen_k, num_q_heads, head_dim, partition_size))
+
+
+def _parse_plan(line: str) -> dict:
+    return dict(kv.split("=", 1) for kv in line.split())
+
+
+def pa_describe_plan(num_seqs: int, total_q: int, max_seqlen_q: int, max_seqlen_k: int,
+                     num_q_heads: int, num_kv_heads: int, head_dim: int, partition_size: int,
+                     dtype, sm_count: int, quantised: bool = False) -> dict:
+    """The launches an attention call with these sizes makes (host only), as a
+    dict of the library's key=value plan line.  dtype: "bf16", "f32" or a
+    torch dtype."""
+    buf = ctypes.create_string_buffer(512)
+    st = load_library().pa_describe_plan(num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+                                         num_q_heads, num_kv_heads, head_dim, partition_size,
+                                         {"bf16": PA_BF16, "f32": PA_F32}.get(dtype, None)
+                                         if isinstance(dtype, str) else _DTYPES[dtype],
+                                         int(bool(quantised)), sm_count, buf, 512)
+    _check(st, "pa_describe_plan")
+    return _parse_plan(buf.value.decode())
+
+
+def pa_last_plan() -> dict:
+    """The plan of the last attention call this thread launched ({} before any)."""
+    line = load_library().pa_last_plan().decode()
+    return {} if line == "none" else _parse_plan(line)
 
 
 def pa_choose_partition_size(num_seqs: int, num_kv_heads: int, max_seqlen_k: int,

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -161,6 +162,101 @@ SplitLayout split_layout(int num_seqs, int max_parts, int num_q_heads, int head_
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// The launches of one attention call, from its sizes alone (host arithmetic;
+// the calls below launch exactly this).
+struct LaunchPlan {
+    bool quantised = false;    // pa_varlen_attention_fp8kv
+    int partition_size = 0;    // split-KV partition used, 0: none
+    int max_parts = 1;         // partitions per request
+    bool tc_decode = false;    // single-query rows on a persistent tensor-core kernel
+    int decode_grid[3] = {0, 0, 0};
+    bool mq = false;           // rows of multi-query requests
+    bool mq_tc = false;        // ... on the persistent tensor-core kernel
+    int mq_grid[3] = {0, 0, 0};
+    bool reduce = false;
+    int reduce_grid[2] = {0, 0};
+    size_t workspace = 0;      // bytes the call needs
+    int head_dim = 0, group = 0;
+    pa_dtype dtype = PA_BF16;
+};
+
+LaunchPlan plan_attention(int num_seqs, int64_t total_q, int max_seqlen_q, int max_seqlen_k,
+                          int num_q_heads, int num_kv_heads, int head_dim, int partition_size,
+                          pa_dtype dtype, bool quantised, int sm_count) {
+    LaunchPlan L;
+    L.quantised = quantised;
+    L.head_dim = head_dim;
+    L.group = num_q_heads / num_kv_heads;
+    L.dtype = dtype;
+    const int sms = sm_count > 0 ? sm_count : 148;
+    const int P = pa_choose_partition_size(num_seqs, num_kv_heads, max_seqlen_k, partition_size,
+                                           sms);
+    L.partition_size = P;
+    L.max_parts = (P > 0 && max_seqlen_k > 0) ? ceil_div(max_seqlen_k, P) : 1;
+    L.tc_decode = quantised || (dtype == PA_BF16 && (head_dim == 128 || head_dim == 256));
+    if (L.tc_decode) {
+        const int64_t items_max = (int64_t)num_seqs * num_kv_heads * L.max_parts;
+        L.decode_grid[0] = (int)std::min<int64_t>(std::min<int64_t>(sms, kMaxDecodeCtas),
+                                                  items_max);
+        L.decode_grid[1] = L.decode_grid[2] = 1;
+    } else {
+        L.decode_grid[0] = L.max_parts;
+        L.decode_grid[1] = num_kv_heads;
+        L.decode_grid[2] = num_seqs;
+    }
+    L.mq = max_seqlen_q > 1;
+    L.mq_tc = L.mq && dtype == PA_BF16 && !quantised;
+    if (L.mq_tc) {
+        const int bq = tc_block_rows(L.group);
+        const int64_t units_max = (total_q / bq + num_seqs) * (int64_t)num_kv_heads;
+        L.mq_grid[0] = (int)std::min<int64_t>(sms, units_max);
+        L.mq_grid[1] = L.mq_grid[2] = 1;
+    } else if (L.mq) {
+        L.mq_grid[0] = (int)total_q;
+        L.mq_grid[1] = num_kv_heads;
+        L.mq_grid[2] = 1;
+    }
+    L.reduce = P > 0;
+    if (L.reduce) {
+        L.reduce_grid[0] = num_seqs;
+        L.reduce_grid[1] = num_q_heads;
+    }
+    if (L.mq_tc || P > 0)
+        L.workspace = align256(plan_bytes(num_seqs)) +
+                      (P > 0 ? split_layout(num_seqs, L.max_parts, num_q_heads, head_dim).total
+                             : 0);
+    return L;
+}
+
+// One line, key=value, of a plan (what pa_describe_plan and pa_last_plan return).
+void format_plan(const LaunchPlan &L, char *buf, size_t n) {
+    const char *dec = L.quantised   ? "paged_decode_tc_fp8"
+                      : L.tc_decode ? "paged_decode_tc"
+                                    : "paged_decode";
+    const char *mq = !L.mq ? "none" : L.mq_tc ? "paged_prefill_tc" : "paged_decode_rows";
+    snprintf(buf, n,
+             "dtype=%s cache=%s head_dim=%d group=%d partition=%d max_parts=%d "
+             "decode_kernel=%s decode_grid=%dx%dx%d mq_kernel=%s mq_grid=%dx%dx%d "
+             "reduce=%s reduce_grid=%dx%d workspace=%zu",
+             L.dtype == PA_F32 ? "f32" : "bf16", L.quantised ? "e4m3" : "plain", L.head_dim,
+             L.group, L.partition_size, L.max_parts, dec, L.decode_grid[0], L.decode_grid[1],
+             L.decode_grid[2], mq, L.mq_grid[0], L.mq_grid[1], L.mq_grid[2],
+             L.reduce ? "split_reduce" : "none", L.reduce_grid[0], L.reduce_grid[1], L.workspace);
+}
+
+thread_local char g_last_plan[512] = "none";
+
+// Records the plan of the call being launched; with PA_DEBUG=1 in the
+// environment, also prints it to stderr.
+void record_plan(const LaunchPlan &L) {
+    static const bool debug = [] {
+        const char *v = getenv("PA_DEBUG");
+        return v && v[0] && strcmp(v, "0") != 0;
+    }();
+    format_plan(L, g_last_plan, sizeof g_last_plan);
+    if (debug) fprintf(stderr, "pa: %s\n", g_last_plan);
+}
+
 // This step's K/V rows for pa_scatter_and_attend (one per query row).
 struct StepScatter {
     const void *key;
@@ -191,6 +287,28 @@ PA_API const char *pa_status_string(pa_status s) {
 }
 
 PA_API const char *pa_last_error_string(void) { return g_last_error; }
+
+PA_API pa_status pa_describe_plan(int num_seqs, int64_t total_q, int max_seqlen_q,
+                                  int max_seqlen_k, int num_q_heads, int num_kv_heads,
+                                  int head_dim, int partition_size, pa_dtype dtype, int quantised,
+                                  int sm_count, char *buf, size_t buf_len) {
+    if (!buf || buf_len == 0) return PA_ERR_INVALID_ARG;
+    buf[0] = 0;
+    if ((dtype != PA_F32 && dtype != PA_BF16) || num_seqs <= 0 || total_q <= 0 ||
+        max_seqlen_q < 0 || max_seqlen_k < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || head_dim <= 0 || partition_size < -1 ||
+        (quantised && dtype != PA_BF16)) {
+        snprintf(g_last_error, sizeof g_last_error, "pa_describe_plan: invalid sizes");
+        return PA_ERR_INVALID_ARG;
+    }
+    format_plan(plan_attention(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_q_heads,
+                               num_kv_heads, head_dim, partition_size, dtype, quantised != 0,
+                               sm_count),
+                buf, buf_len);
+    return PA_OK;
+}
+
+PA_API const char *pa_last_plan(void) { return g_last_plan; }
 
 PA_API const char *pa_build_info(void) {
     return "libpa paged varlen attention; sm_103a; kernels: reshape_and_cache, "
@@ -329,9 +447,11 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     // ---- split plan and workspace
-    const int P = pa_choose_partition_size(num_seqs, num_kv_heads, max_seqlen_k, partition_size,
-                                           dev.sm_count);
-    const int max_parts = (P > 0 && max_seqlen_k > 0) ? ceil_div(max_seqlen_k, P) : 1;
+    const LaunchPlan plan = plan_attention(num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+                                           num_q_heads, num_kv_heads, head_dim, partition_size,
+                                           dtype, false, dev.sm_count);
+    const int P = plan.partition_size;
+    const int max_parts = plan.max_parts;
     float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
     float *xpart_o = nullptr, *xpart_m = nullptr, *xpart_l = nullptr;
     int4 *cut_tab = nullptr;
@@ -341,12 +461,11 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         return PA_ERR_UNSUPPORTED;
     }
     // the workspace: the multi-query kernel's unit plan, then the split partials
-    const bool mq_tc = max_seqlen_q > 1 && dtype == PA_BF16;
+    const bool mq_tc = plan.mq_tc;
     const size_t plan_sz = align256(plan_bytes(num_seqs));
-    int *plan = nullptr;
+    int *unit_plan = nullptr;
     if (mq_tc || P > 0) {
-        const size_t need =
-            plan_sz + (P > 0 ? split_layout(num_seqs, max_parts, num_q_heads, head_dim).total : 0);
+        const size_t need = plan.workspace;
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) {
             snprintf(g_last_error, sizeof g_last_error,
                      "this call needs %zu bytes of 16-byte aligned workspace (split-KV "
@@ -355,7 +474,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
                      workspace && !aligned16(workspace) ? " (misaligned)" : "");
             return PA_ERR_WORKSPACE;
         }
-        plan = static_cast<int *>(workspace);
+        unit_plan = static_cast<int *>(workspace);
     }
     if (P > 0) {
         const SplitLayout L = split_layout(num_seqs, max_parts, num_q_heads, head_dim);
@@ -425,9 +544,10 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
     // 0) this step's K/V rows (pa_scatter_and_attend): the scatter kernel; the
     //    tensor-core decode kernel launched next overlaps it (programmatic
     //    dependent launch) and only its K/V loads wait for it
-    const bool tc_decode = dtype == PA_BF16 && (head_dim == 128 || head_dim == 256);
+    const bool tc_decode = plan.tc_decode;
     int dtc_grid = 0;   // CTAs of the tensor-core decode kernel (0: not launched)
     cudaError_t ce;
+    record_plan(plan);
     if (fs) {
         const int64_t eb = dtype == PA_F32 ? 4 : 2;
         ce = launch_reshape_and_cache(fs->key, fs->value, fs->stride * eb, const_cast<void *>(key_cache),
@@ -477,16 +597,14 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         da.xpart_m = xpart_m;
         da.xpart_l = xpart_l;
         da.cut_tab = cut_tab;
-        const int64_t items_max = (int64_t)num_seqs * num_kv_heads * max_parts;
-        const int grid = (int)std::min<int64_t>(
-            std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, kMaxDecodeCtas), items_max);
+        const int grid = plan.decode_grid[0];
         dtc_grid = grid;
         ce = head_dim == 128 ? launch_decode_tc_d128(group, qmap_d, kmap_d, vmap_d, da, grid, s)
                              : launch_decode_tc_d256(group, qmap_d, kmap_d, vmap_d, da, grid, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode_tc launch");
     } else {
         a.mode = 0;
-        ce = launch(dim3(max_parts, num_kv_heads, num_seqs));
+        ce = launch(dim3(plan.decode_grid[0], plan.decode_grid[1], plan.decode_grid[2]));
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_decode launch");
     }
     // 2) rows of multi-query requests (verify windows, prefill chunks): bf16 on
@@ -514,7 +632,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         pl.block_rows = bq;
         pl.tile_keys = tc_tile_keys(head_dim);
         pl.max_keys = max_blocks_per_seq * block_size;
-        pl.plan = plan;
+        pl.plan = unit_plan;
         ce = launch_mq_plan(pl, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "mq_plan launch");
         // 2) the persistent multi-query kernel: at most one CTA per SM, no more
@@ -534,11 +652,10 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         ta.causal = causal ? 1 : 0;
         ta.box_rows = tc_box;
         ta.err = dev.err;
-        ta.plan = plan;
+        ta.plan = unit_plan;
         ta.test_skip_first_k = g_expire_next_wait.exchange(0);
         ta.total_q = total_q;
-        const int64_t units_max = (total_q / bq + num_seqs) * (int64_t)num_kv_heads;
-        const int grid = (int)std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, units_max);
+        const int grid = plan.mq_grid[0];
         switch (head_dim) {
             case 64: ce = launch_prefill_tc_d64(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
             case 128: ce = launch_prefill_tc_d128(group, qmap, kmap_tc, vmap_tc, ta, grid, s); break;
@@ -547,7 +664,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_prefill_tc launch");
     } else if (max_seqlen_q > 1) {
         a.mode = 1;
-        ce = launch(dim3((unsigned)total_q, num_kv_heads, 1));
+        ce = launch(dim3((unsigned)plan.mq_grid[0], plan.mq_grid[1], 1));
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_rows launch");
     }
     // 3) merge the split partials of the single-query requests
@@ -786,9 +903,11 @@ PA_API pa_status pa_varlen_attention_fp8kv(
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     // split plan and workspace: the same layout as pa_varlen_attention's
-    const int P = pa_choose_partition_size(num_seqs, num_kv_heads, max_seqlen_k, partition_size,
-                                           dev.sm_count);
-    const int max_parts = (P > 0 && max_seqlen_k > 0) ? ceil_div(max_seqlen_k, P) : 1;
+    const LaunchPlan plan = plan_attention(num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+                                           num_q_heads, num_kv_heads, head_dim, partition_size,
+                                           dtype, true, dev.sm_count);
+    const int P = plan.partition_size;
+    const int max_parts = plan.max_parts;
     if (P > 0 && max_parts > kMaxReduceParts) {
         snprintf(g_last_error, sizeof g_last_error,
                  "%d split-KV partitions per request, at most %d", max_parts, kMaxReduceParts);
@@ -800,7 +919,7 @@ PA_API pa_status pa_varlen_attention_fp8kv(
     if (P > 0) {
         const size_t plan_sz = align256(plan_bytes(num_seqs));
         const SplitLayout L = split_layout(num_seqs, max_parts, num_q_heads, head_dim);
-        const size_t need = plan_sz + L.total;
+        const size_t need = plan.workspace;
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) {
             snprintf(g_last_error, sizeof g_last_error,
                      "this call needs %zu bytes of 16-byte aligned workspace (split-KV "
@@ -897,9 +1016,8 @@ PA_API pa_status pa_varlen_attention_fp8kv(
     da.k_scales = key_scales;
     da.v_scales = value_scales;
     da.num_blocks = num_blocks;
-    const int64_t items_max = (int64_t)num_seqs * num_kv_heads * max_parts;
-    const int grid = (int)std::min<int64_t>(
-        std::min<int64_t>(dev.sm_count > 0 ? dev.sm_count : 148, kMaxDecodeCtas), items_max);
+    const int grid = plan.decode_grid[0];
+    record_plan(plan);
     cudaError_t ce =
         head_dim == 128 ? launch_decode_tc_fp8_d128(group, qmap_d, kmap_d, vmap_d, da, grid, s)
                         : launch_decode_tc_fp8_d256(group, qmap_d, kmap_d, vmap_d, da, grid, s);
@@ -907,7 +1025,7 @@ PA_API pa_status pa_varlen_attention_fp8kv(
     // rows of multi-query requests: one CTA per (row, KV head)
     if (max_seqlen_q > 1) {
         a.mode = 1;
-        ce = launch(dim3((unsigned)total_q, num_kv_heads, 1));
+        ce = launch(dim3((unsigned)plan.mq_grid[0], plan.mq_grid[1], 1));
         if (ce != cudaSuccess) return cuda_fail(ce, "paged_rows (quantised) launch");
     }
     if (P > 0) {

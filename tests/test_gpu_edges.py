@@ -174,3 +174,38 @@ def test_padded_layout_matches_oracle(D, Hq, Hkv):
     w = wl.padded(small)
     assert len(set(w.q_lens.tolist())) == 1 and w.total_q == w.num_seqs * int(w.q_lens[0])
     check_step(w)
+
+
+@pytest.mark.parametrize("D,dtype", [(128, wl.BF16), (64, wl.F32)])
+def test_launch_plan_recorded_and_logged(D, dtype):
+    """A real call records the plan pa_describe_plan gives for its sizes on
+    this GPU, and with PA_DEBUG=1 prints it to stderr (a child process, so
+    the variable is read at its first call)."""
+    import os
+    import subprocess
+    import sys
+    w = wl.random_small(515 + D, dtype=dtype, num_seqs=6, num_q_heads=8, num_kv_heads=2,
+                        head_dim=D, max_prior=700, max_q=7)
+    dw = DeviceWorkload(w)
+    dw.scatter()
+    dw.attention(partition_size=256)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    want = pa.pa_describe_plan(w.num_seqs, w.total_q, w.max_seqlen_q, w.max_seqlen_k,
+                               w.num_q_heads, w.num_kv_heads, D, 256, dtype, sms)
+    assert pa.pa_last_plan() == want
+    assert want["mq_kernel"] == ("paged_prefill_tc" if dtype == wl.BF16 else "paged_decode_rows")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys; sys.path.insert(0, %r); sys.path.insert(0, %r)\n"
+            "from harness import DeviceWorkload\n"
+            "from paged_kv_varlen_gb300 import workloads as wl\n"
+            "w = wl.random_small(%d, dtype=%r, num_seqs=6, num_q_heads=8, num_kv_heads=2,"
+            " head_dim=%d, max_prior=700, max_q=7)\n"
+            "dw = DeviceWorkload(w); dw.scatter(); dw.attention(partition_size=256)\n"
+            "import torch; torch.cuda.synchronize()\n"
+            % (root, os.path.join(root, "tests"), 515 + D, dtype, D))
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, PA_DEBUG="1"),
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l[4:] for l in r.stderr.splitlines() if l.startswith("pa: ")]
+    assert lines and dict(kv.split("=", 1) for kv in lines[-1].split()) == want
