@@ -62,8 +62,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # command in profiles/paged_decode_tc_kernel__gqa_decode_bf16.md) of the
 # kernel sources whose hash is recorded beside it: the files that define that
 # kernel.  Reported as null once they change, until a new capture is taken.
-NCU_TRAFFIC = {"sources_sha256": "d3429d45005de5736aa6f83c597123fbdc0d7f80fa4a1384a92ff3edd2021eeb",
-               "bytes_per_launch": 526285312 + 5297152, "workload": 1,
+NCU_TRAFFIC = {"sources_sha256": "dca46030aa4db0d670f5ec30ba726a4da3ec61fc15df18fa9a3092338e4a66e8",
+               "bytes_per_launch": 526283776 + 5068800, "workload": 1,
                "kernel": "paged_decode_tc_kernel"}
 TRAFFIC_SOURCES = ("decode_tc.cuh", "decode_tc_d128.cu", "pa_common.cuh", "tc_common.cuh")
 

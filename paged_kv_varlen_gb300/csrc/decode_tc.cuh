@@ -45,7 +45,11 @@
 //    K/V rows), only before the K/V loads, so its setup, work plan and first
 //    page ids overlap the scatter -- and lets the next kernel (the reduce)
 //    be scheduled from its start.
-//  * Every barrier wait is bounded (pa::mbar_wait); nothing spins forever.
+//  * Every barrier wait is bounded (pa::mbar_wait_ool); nothing spins forever.
+//    The waits' retry loop is out of line, one copy for all wait sites: the
+//    smaller code (114 -> 105 KB) measured 107.4 -> 104.0 us on the GQA decode
+//    batch.  (Taking the item iterator or the item store out of line as well
+//    was slower: their structures then live on the stack.)
 #pragma once
 
 #include <climits>
@@ -662,7 +666,7 @@ __global__ void __launch_bounds__(288, 1)
             if (lane == 0 && is_k && ph == 0 && j == 0) {   // Q^T of the item: its G heads
                 const int qb = itn & 1;
                 if (itn >= 2)
-                    bad = !mbar_wait(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1, a.err,
+                    bad = !mbar_wait_ool(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1, a.err,
                                      abort_flag);
                 if (!bad) {
                     mbar_arrive_expect_tx(bar_q_full + 8 * qb, C::KCH * G * 128);
@@ -687,7 +691,7 @@ __global__ void __launch_bounds__(288, 1)
                 const int slot = idx % C::NR;
                 if (lane == 0 && !bad) {
                     if (idx >= C::NR)
-                        bad = !mbar_wait(bempty + 8 * slot, ((idx / C::NR) - 1) & 1, a.err,
+                        bad = !mbar_wait_ool(bempty + 8 * slot, ((idx / C::NR) - 1) & 1, a.err,
                                          abort_flag);
                     if (!bad) mbar_arrive_expect_tx(bfull + 8 * slot, (u1 - u0) * BR * 256);
                 }
@@ -719,11 +723,11 @@ __global__ void __launch_bounds__(288, 1)
             // O^T[ob] (+)= V^T . P^T for global tile g_t
             auto issue_pv = [&](int g_t, int ob, bool first, bool last) {
                 const int pb = g_t & 1;
-                mbar_wait(bar_p_full + 8 * pb, (g_t >> 1) & 1, a.err, abort_flag);
+                mbar_wait_ool(bar_p_full + 8 * pb, (g_t >> 1) & 1, a.err, abort_flag);
 #pragma unroll
                 for (int c = 0; c < C::KS; ++c) {
                     const int idx = g_t * C::KS + c;
-                    mbar_wait(bar_v_full + 8 * (idx % C::NR), (idx / C::NR) & 1, a.err,
+                    mbar_wait_ool(bar_v_full + 8 * (idx % C::NR), (idx / C::NR) & 1, a.err,
                               abort_flag);
                 }
                 tc_fence_after();
@@ -760,16 +764,16 @@ __global__ void __launch_bounds__(288, 1)
                 }
                 const int qb = itn & 1;
                 const int ob = itn & 1;
-                mbar_wait(bar_q_full + 8 * qb, (itn >> 1) & 1, a.err, abort_flag);
+                mbar_wait_ool(bar_q_full + 8 * qb, (itn >> 1) & 1, a.err, abort_flag);
                 const uint32_t qs = q_smem + qb * C::Q_BUF;
                 for (int j = 0; j < cur.ntiles; ++j) {
                     const int sb = gt & 1;
                     if (gt >= 2)
-                        mbar_wait(bar_s_free + 8 * sb, ((gt >> 1) - 1) & 1, a.err, abort_flag);
+                        mbar_wait_ool(bar_s_free + 8 * sb, ((gt >> 1) - 1) & 1, a.err, abort_flag);
 #pragma unroll
                     for (int c = 0; c < C::KS; ++c) {
                         const int idx = gt * C::KS + c;
-                        mbar_wait(bar_k_full + 8 * (idx % C::NR), (idx / C::NR) & 1, a.err,
+                        mbar_wait_ool(bar_k_full + 8 * (idx % C::NR), (idx / C::NR) & 1, a.err,
                                   abort_flag);
                     }
                     tc_fence_after();
@@ -829,7 +833,7 @@ __global__ void __launch_bounds__(288, 1)
             }
             for (int j = 0; j < cur.ntiles; ++j) {
                 const int sb = gt & 1;
-                mbar_wait(bar_s_full + 8 * sb, (gt >> 1) & 1, a.err, abort_flag);
+                mbar_wait_ool(bar_s_full + 8 * sb, (gt >> 1) & 1, a.err, abort_flag);
                 tc_fence_after();
                 float sv[8];
                 tmem_ld8(t_lane + C::S_COL + sb * C::NP, sv);
@@ -871,7 +875,7 @@ __global__ void __launch_bounds__(288, 1)
                     for (int g = 0; g < G; ++g)
                         if (need[g]) f[g] = m_ref[g] == -INFINITY ? 0.f : exp2f(m_ref[g] - mnew[g]);
                     if (j >= 1) {   // O^T holds PVs of this item: rescale after the last one
-                        mbar_wait(bar_o_done + 8 * ((gt - 1) & 1), ((gt - 1) >> 1) & 1, a.err,
+                        mbar_wait_ool(bar_o_done + 8 * ((gt - 1) & 1), ((gt - 1) >> 1) & 1, a.err,
                                   abort_flag);
                         tc_fence_after();
 #pragma unroll
@@ -902,7 +906,7 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
                     for (int c = 0; c < C::KS; ++c) {
                         const int idx = gt * C::KS + c;
-                        mbar_wait(bar_v_full + 8 * (idx % C::NR), (idx / C::NR) & 1, a.err,
+                        mbar_wait_ool(bar_v_full + 8 * (idx % C::NR), (idx / C::NR) & 1, a.err,
                                   abort_flag);
                         if (!kv) {
                             uint4 *r0 = reinterpret_cast<uint4 *>(
@@ -920,7 +924,7 @@ __global__ void __launch_bounds__(288, 1)
                 // P^T buffer pb was last read by PV(gt - 2)
                 const int pb = gt & 1;
                 if (gt >= 2)
-                    mbar_wait(bar_o_done + 8 * pb, ((gt >> 1) - 1) & 1, a.err, abort_flag);
+                    mbar_wait_ool(bar_o_done + 8 * pb, ((gt >> 1) - 1) & 1, a.err, abort_flag);
                 uint8_t *prow = smem + C::OFF_P + pb * C::P_BUF + (t >> 6) * (C::NP * 128);
                 const int kc = t & 63;
 #pragma unroll
@@ -954,7 +958,7 @@ __global__ void __launch_bounds__(288, 1)
             }
             float o[C::KS][8];
             if (cur.ntiles > 0) {
-                mbar_wait(bar_o_full + 8 * ob, (itn >> 1) & 1, a.err, abort_flag);
+                mbar_wait_ool(bar_o_full + 8 * ob, (itn >> 1) & 1, a.err, abort_flag);
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < C::KS; ++c)
