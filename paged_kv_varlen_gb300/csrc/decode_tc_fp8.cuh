@@ -65,7 +65,8 @@ struct DtcF8Cfg {
     static constexpr int NRV = D >= 256 ? 2 : 3;   // bf16 V stages
     static constexpr int NSC = 3;                  // scale stages (tiles)
     static constexpr int Q_BUF = KCH * NP * 128;   // bf16 Q^T: [KCH][16 rows][128 B]
-    static constexpr int Q8_BUF = KS * 2 * NP * 128;   // E4M3 Q^T: [KS][hi 16 rows, lo 16 rows][128 B]
+    // E4M3 Q^T: [KS][hi 16 rows, lo 16 rows][128 B]
+    static constexpr int Q8_BUF = KS * 2 * NP * 128;
     static constexpr int P_BUF = 2 * NP * 128;
     static constexpr int OFF_KC = 0;
     static constexpr int OFF_VC = NRC * CSLOT;
@@ -143,7 +144,8 @@ __device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint16_t &hi, u
 // E4M3 value, subnormals included, is an f16): lo = codes 0, 1 and hi = codes
 // 2, 3, the lower code in the low half.
 __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    const __half2_raw l = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
+    const __half2_raw l =
+        __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
     lo = (uint32_t)l.x | ((uint32_t)l.y << 16);
     hi = (uint32_t)h.x | ((uint32_t)h.y << 16);
@@ -307,11 +309,11 @@ __global__ void __launch_bounds__(480, 1)
 
     if (warp == 4 || warp == 5 || warp == 7 || warp == 8 || warp == 13) {
         // ============================================================ streaming warps
-        // Warps 4 and 7 stream K codes, warps 5 and 8 V codes: warp ph of a ring takes page runs [0, h0)
-        // (ph 0) or [h0, nbox) (ph 1) of every stage, one 128-code box per run
-        // and lane.  Warp 13 copies each key's K and V scale.  Lanes fetch the
-        // page ids of each tile into a shared ring by 4-byte cp.async three
-        // tiles ahead, so no load is waited on.
+        // Warps 4 and 7 stream K codes, warps 5 and 8 V codes: warp ph of a
+        // ring takes page runs [0, h0) (ph 0) or [h0, nbox) (ph 1) of every
+        // stage, one 128-code box per run and lane.  Warp 13 copies each key's
+        // K and V scale.  Lanes fetch the page ids of each tile into a shared
+        // ring by 4-byte cp.async three tiles ahead, so no load is waited on.
         const bool is_sc = warp == 13;
         const bool is_k = warp == 4 || warp == 7;
         const int ph = warp >= 7 ? 1 : 0;
@@ -444,7 +446,8 @@ __global__ void __launch_bounds__(480, 1)
             if (lane == 0) {
                 bool ok = true;
                 if (itn >= 2)
-                    ok = mbar_wait_ool(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1, a.err, abort_flag);
+                    ok = mbar_wait_ool(bar_q_empty + 8 * qb, ((itn >> 1) - 1) & 1, a.err,
+                                       abort_flag);
                 if (ok) {
                     mbar_arrive_expect_tx(bar_q_full + 8 * qb, C::KCH * G * 128);
 #pragma unroll
@@ -534,7 +537,8 @@ __global__ void __launch_bounds__(480, 1)
                 const int vsl = idx % C::NRV;
                 mbar_wait_ool(bar_vc_full + 8 * cs, (idx / C::NRC) & 1, a.err, abort_flag);
                 if (idx >= C::NRV)
-                    mbar_wait_ool(bar_v_empty + 8 * vsl, ((idx / C::NRV) - 1) & 1, a.err, abort_flag);
+                    mbar_wait_ool(bar_v_empty + 8 * vsl, ((idx / C::NRV) - 1) & 1, a.err,
+                                  abort_flag);
                 const uint32_t row = vcring + cs * C::CSLOT + r * 128;
                 const uint32_t vdst = vring + vsl * C::VSLOT + r * 128;
                 // all eight loads first: the stores below are ordered after them
