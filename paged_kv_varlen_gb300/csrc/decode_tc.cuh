@@ -10,7 +10,7 @@
 //
 // GB300 design (persistent: one CTA per SM, 224 threads)
 //  * A work item is (request, KV head, partition).  Every CTA scans the batch
-//    once, weighs each item by five per key tile plus three (an item's fixed
+//    once, weighs each item by five per key tile plus three (item_cost; an item's fixed
 //    cost -- Q load, pipeline turn, epilogue -- measured at about 0.6 tile), and
 //    takes, in order, the items whose cumulative work starts inside its
 //    1/gridDim share.
@@ -96,7 +96,7 @@ struct DtcCfg {
 };
 
 // Work of one decode request: its (partition, KV head) items, ordered
-// partition-major, each weighed by five per key tile plus three.
+// partition-major, each weighed by five per key tile plus a.item_cost.
 struct DtcReq {
     int items;   // 0 when the request has no decode work here
     int np;      // partitions
@@ -118,11 +118,11 @@ __device__ __forceinline__ DtcReq dtc_request_from(const DecodeTcArgs &a, int c0
         q.N = N;
         q.np = (N + P - 1) / P;
         if (q.np == 0) return q;                      // no keys: the reduce writes zeros
-        q.wfull = 5 * ((P + 127) / 128) + 3;
-        q.wlast = 5 * ((N - (q.np - 1) * P + 127) / 128) + 3;
+        q.wfull = 5 * ((P + 127) / 128) + a.item_cost;
+        q.wlast = 5 * ((N - (q.np - 1) * P + 127) / 128) + a.item_cost;
     } else {
         q.np = 1;                                     // one item, even with no keys
-        q.wfull = q.wlast = 5 * ((N + 127) / 128) + 3;
+        q.wfull = q.wlast = 5 * ((N + 127) / 128) + a.item_cost;
     }
     q.items = q.np * a.num_kv_heads;
     return q;
@@ -220,10 +220,10 @@ __device__ __forceinline__ void dtc_next(const DecodeTcArgs &a, DtcIter &it, con
 // *j (in [0, tiles of k)), *start being item k's start; k == q.items when the
 // boundary falls at the request's end.  With split partials an item of two or
 // more tiles is cut at the tile boundary nearest to `off` (items weigh five
-// per tile plus three); otherwise an item goes whole to the side its start
+// per tile plus item_cost); otherwise an item goes whole to the side its start
 // lies on.
-__device__ __forceinline__ int dtc_cut(const DtcReq &q, int hkv, bool split, int64_t off, int *j,
-                                       int64_t *start) {
+__device__ __forceinline__ int dtc_cut(const DtcReq &q, int hkv, int item_cost, bool split,
+                                       int64_t off, int *j, int64_t *start) {
     const int64_t nf = (int64_t)(q.np - 1) * hkv;   // items of full partitions
     const int64_t wf = nf * q.wfull;
     int64_t k, st;
@@ -237,7 +237,7 @@ __device__ __forceinline__ int dtc_cut(const DtcReq &q, int hkv, bool split, int
         st = wf + (k - nf) * q.wlast;
         w = q.wlast;
     }
-    const int n = (w - 3) / 5;   // the item's tiles
+    const int n = (w - item_cost) / 5;   // the item's tiles
     int jj;
     if (split && n >= 2) jj = (int)(((off - st) * 2 * n + w) / (2 * w));   // nearest boundary
     else jj = off == st ? 0 : n;
@@ -337,7 +337,7 @@ __device__ __forceinline__ void dtc_plan_share(const DecodeTcArgs &a, const DtcP
         // GQA decode batch of 4-tile items, and to gain ~3.5 % on a batch of
         // 8-tile items at 8 items per CTA.
         const bool cut_items =
-            split && W / nb < 10 * (5 * (int64_t)((a.partition_size + 127) / 128) + 3);
+            split && W / nb < 10 * (5 * (int64_t)((a.partition_size + 127) / 128) + a.item_cost);
         // request r (cumulative work E, total w) containing lo or hi; the one
         // containing lo also warms L2 with the block-table entries of the first
         // tiles (the producers fetch them next)
@@ -346,7 +346,7 @@ __device__ __forceinline__ void dtc_plan_share(const DecodeTcArgs &a, const DtcP
             if (E <= lo && lo < E + w) {
                 int j;
                 int64_t st;
-                const int k = dtc_cut(q, hkv, cut_items, lo - E, &j, &st);
+                const int k = dtc_cut(q, hkv, a.item_cost, cut_items, lo - E, &j, &st);
                 plan_rk[0] = r;
                 plan_rk[1] = k;
                 plan_s[0] = E + st;
@@ -362,7 +362,7 @@ __device__ __forceinline__ void dtc_plan_share(const DecodeTcArgs &a, const DtcP
             if (E <= hi && hi < E + w) {
                 int j;
                 int64_t st;
-                const int k = dtc_cut(q, hkv, cut_items, hi - E, &j, &st);
+                const int k = dtc_cut(q, hkv, a.item_cost, cut_items, hi - E, &j, &st);
                 plan_s[1] = E + st;
                 plan_j[1] = j;
                 if (j > 0) {

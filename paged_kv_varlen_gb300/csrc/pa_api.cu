@@ -593,6 +593,7 @@ static pa_status attention_impl(void *out, const void *q, const void *key_cache,
         da.box_rows = dbox;
         da.err = dev.err;
         da.after_scatter = fs != nullptr ? 1 : 0;
+        da.item_cost = 3;   // ~0.6 tile (the bf16 kernel's Q load, pipeline turn, epilogue)
         da.xpart_o = xpart_o;
         da.xpart_m = xpart_m;
         da.xpart_l = xpart_l;
@@ -1016,6 +1017,9 @@ PA_API pa_status pa_varlen_attention_fp8kv(
     da.k_scales = key_scales;
     da.v_scales = value_scales;
     da.num_blocks = num_blocks;
+    // an item costs ~5 tiles beyond its keys here (Q split, deferred output,
+    // the roles' item changes; per-CTA times fitted on the GQA decode batch)
+    da.item_cost = 25;
     const int grid = plan.decode_grid[0];
     record_plan(plan);
     cudaError_t ce =

@@ -123,6 +123,10 @@ struct DecodeTcArgs {
     const float *k_scales;
     const float *v_scales;
     int64_t num_blocks;
+    // weight of an item's fixed cost in the work plan, in units of a fifth of
+    // a key tile (an item weighs 5 per tile plus this): what one item costs
+    // beyond its tiles on the kernel in question, measured
+    int item_cost;
 };
 
 // Keys per K/V tile of the multi-query kernel, keys of one V sub-tile (the
