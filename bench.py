@@ -62,8 +62,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # command in profiles/paged_decode_tc_kernel__gqa_decode_bf16.md) of the
 # kernel sources whose hash is recorded beside it: the files that define that
 # kernel.  Reported as null once they change, until a new capture is taken.
-NCU_TRAFFIC = {"sources_sha256": "dca46030aa4db0d670f5ec30ba726a4da3ec61fc15df18fa9a3092338e4a66e8",
-               "bytes_per_launch": 526283776 + 5068800, "workload": 1,
+NCU_TRAFFIC = {"sources_sha256": "79bb8d8ff887ab01c86416183e78737d3549c5267180b728c53ea436b1267083",
+               "bytes_per_launch": 526288384 + 4950528, "workload": 1,
                "kernel": "paged_decode_tc_kernel"}
 TRAFFIC_SOURCES = ("decode_tc.cuh", "decode_tc_d128.cu", "pa_common.cuh", "tc_common.cuh")
 
