@@ -85,3 +85,31 @@ def test_no_call_no_last_plan():
     t.start()
     t.join()
     assert seen == [{}]
+
+
+def test_workspace_query_covers_every_plan():
+    """pa_varlen_attention_workspace_size (which has no SM count) is enough for
+    the plan of any GPU size: random batch shapes, partition sizes -1 / 0 /
+    forced, SM counts from 1 to 256, plain and quantised caches."""
+    import random
+    rnd = random.Random(5)
+    for _ in range(3000):
+        S = rnd.randint(1, 300)
+        Hkv = rnd.choice([1, 2, 4, 8])
+        Hq = Hkv * rnd.randint(1, 8)
+        D = rnd.choice([64, 128, 256])
+        max_k = rnd.choice([0, 1, 100, 600, 4096, 70000])
+        max_q = rnd.choice([1, 1, 5, 300])
+        P = rnd.choice([-1, 0, 0, 32, 256, 512, 1024])
+        dtype = rnd.choice(["bf16", "f32"])
+        quant = dtype == "bf16" and D != 64 and rnd.random() < 0.3
+        sms = rnd.randint(1, 256)
+        total_q = S * max_q
+        p = plan(S, total_q, max_q, max_k, Hq, Hkv, D, P, dtype, sms, quantised=quant)
+        need = int(p["workspace"])
+        have = pa.pa_varlen_attention_workspace_size(S, max_k, Hq, D, P)
+        assert need <= have, (S, Hkv, Hq, D, max_k, max_q, P, dtype, sms, need, have)
+        assert int(p["max_parts"]) >= 1
+        if p["partition"] != "0":
+            assert p["reduce"] == "split_reduce"
+            assert int(p["max_parts"]) == -(-max(max_k, 1) // int(p["partition"])) or max_k == 0
