@@ -61,8 +61,10 @@ struct DtcF8Cfg {
     static constexpr int CSLOT = BN * 128;         // code stage: 128 keys x 128 codes
     static constexpr int VSLOT = BN * 256;         // bf16 V stage: 128 keys x 128 dims
     static constexpr int VSUB = BN * 128;          // one 64-dim sub-chunk of a V stage
-    static constexpr int NRC = 3;                  // stages of each code ring
-    static constexpr int NRV = D >= 256 ? 2 : 3;   // bf16 V stages
+    // stages of each code ring and f16 V stages (at D = 128, 4 + 2 measured
+    // 3.4 % faster than 3 + 3 on the GQA decode batch)
+    static constexpr int NRC = D >= 256 ? 3 : 4;
+    static constexpr int NRV = 2;
     static constexpr int NSC = 3;                  // scale stages (tiles)
     static constexpr int Q_BUF = KCH * NP * 128;   // bf16 Q^T: [KCH][16 rows][128 B]
     // E4M3 Q^T: [KS][hi 16 rows, lo 16 rows][128 B]

@@ -312,7 +312,8 @@ CASES = {
 def test_protocol_has_no_stale_wait_or_overwrite(case):
     items, KS = CASES[case]
     for seed in range(40):
-        simulate(items, KS, seed, NRV=3 if KS == 1 else 2)
+        # the kernel's stage counts: 4 code + 2 f16 V stages at head_dim 128, 3 + 2 at 256
+        simulate(items, KS, seed, NRC=4 if KS == 1 else 3, NRV=2)
 
 
 @pytest.mark.parametrize("mutate", ["no_sc_empty", "no_v_empty", "no_kc_empty", "no_q_empty",
